@@ -1,0 +1,559 @@
+"""Benchmark: split-KV decode over a quantized KV cache on one GB300.
+
+One step = the whole decode hot path for one new token per request:
+quantize-on-append of the new K/V rows, the split-KV partial kernel and the
+combine kernel (split count from kvq_auto_splits), over a cache of kv_len
+tokens per request that is resident in HBM.  The headline workload is GQA
+4:1 FP8: batch 2, 32 query / 8 kv heads, head_dim 128, kv_len 32768, 1% of
+elements x10, bf16 output.
+
+Timing: W warm-up steps, then K timed steps; before every timed step the L2
+is flushed by writing a 256 MiB buffer, and each step is bracketed by CUDA
+events on the launch stream (the three launches are replayed as one CUDA
+graph).  `value` is the mean device time per step in microseconds (lower is
+better); KV GB/s = attended cache bytes / step time.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
+                    [--no-sweep]
+
+With --impl reference the CPU oracle is timed on the same workload on the
+host cores (the reference arm); under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("decode-attention µs/step and KV-cache GB/s (% of GB300 HBM peak) vs kv_len")
+HEADLINE_L = 32768
+FLUSH_BYTES = 256 << 20
+
+
+def env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, ncu traffic
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ["kvq_decode.cu", "kvq_device.cuh", "kvq_internal.h"]:
+        with open(os.path.join(ROOT, "quantized_kv_cache_05_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch of the partial kernel from the committed ncu
+    summary, when it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+class Bench:
+    def __init__(self, w, device, splits=0):
+        import torch
+        from quantized_kv_cache_05_gb300 import kvq, runtime, synth
+        self.torch, self.kvq, self.runtime, self.synth = torch, kvq, runtime, synth
+        self.w, self.device = w, device
+        torch.cuda.set_device(device)
+        self.stream = torch.cuda.Stream(device)
+        B, Hkv, D, L = w.B, w.Hkv, w.D, w.Lmax
+        bt, npages = w.block_table()
+        ps = w.page_size_eff()
+        fmt = runtime.FMT[w.fmt]
+        with torch.cuda.stream(self.stream):
+            # calibrate the static scales on the device (amax kernel)
+            amax = {}
+            self.q = self._bf16(w.q())
+            tensors = [synth.T_K] if w.mla else [synth.T_K, synth.T_V]
+            dev_rows = {}
+            for t in tensors:
+                a = torch.zeros(1, dtype=torch.float32, device=device)
+                m = 0.0
+                rows = []
+                for b in range(B):
+                    x = self._bf16(w.kv_rows(t, b))
+                    kvq.check(kvq.kvq_amax_bf16(x, x.numel(), a, self.stream))
+                    m = max(m, float(a.item()))
+                    rows.append(x)
+                amax[t] = m
+                dev_rows[t] = rows
+            ks = kvq.kvq_tensor_scale(fmt, amax[synth.T_K])[1]
+            vs = kvq.kvq_tensor_scale(fmt, amax.get(synth.T_V, amax[synth.T_K]))[1]
+            self.cache = runtime.QuantizedKVCache(w.fmt, npages, ps, Hkv, D, torch.from_numpy(bt),
+                                                  ks, vs, rope_dim=w.rope, device=device)
+            zero = torch.zeros(1, dtype=torch.int32, device=device)
+            kpe_rows = [self._bf16(w.kpe_rows(b)) for b in range(B)] if w.mla else None
+            for b in range(B):
+                c = self.cache.struct()
+                c.block_table = self.cache.block_table[b].data_ptr()
+                k = dev_rows[synth.T_K][b][None]
+                v = None if w.mla else dev_rows[synth.T_V][b][None]
+                kpe = kpe_rows[b][None] if w.mla else None
+                kvq.check(kvq.kvq_quantize_append(c, k, v, kpe, zero, 1, k.shape[1], self.stream))
+            # the new token of each step: the last row of each request,
+            # re-appended at position L_b - 1 (same work every step)
+            last = [int(x) - 1 for x in w.seq_lens]
+            self.k_new = torch.stack([dev_rows[synth.T_K][b][last[b]:last[b] + 1]
+                                      for b in range(B)]).contiguous()
+            self.v_new = None if w.mla else torch.stack(
+                [dev_rows[synth.T_V][b][last[b]:last[b] + 1] for b in range(B)]).contiguous()
+            self.kpe_new = torch.stack([kpe_rows[b][last[b]:last[b] + 1]
+                                        for b in range(B)]).contiguous() if w.mla else None
+            self.start_pos = torch.tensor(last, dtype=torch.int32, device=device)
+            self.seq_lens = torch.from_numpy(np.ascontiguousarray(w.seq_lens, np.int32)).to(device)
+            del dev_rows, kpe_rows
+        self.stream.synchronize()
+        self.splits = splits or runtime.auto_splits(B, Hkv, w.G, w.Lmax, w.fmt, device)
+        self.out_scale = 1.0
+        if w.out == "e4m3":
+            # calibrate the output scale from an fp32-output pass (amax / 448)
+            cfg32 = self._cfg("f32", 1.0)
+            o = runtime.decode(self.cache, self.q, self.seq_lens, cfg32, None, None, self.stream)
+            a = torch.zeros(1, dtype=torch.float32, device=device)
+            ob = o.to(torch.bfloat16)   # amax over bf16-rounded outputs (calibration only)
+            kvq.check(kvq.kvq_amax_bf16(ob, ob.numel(), a, self.stream))
+            self.out_scale = kvq.kvq_tensor_scale(kvq.KVQ_FP8_E4M3, float(a.item()) * 1.01)[1]
+        self.cfg = self._cfg(w.out, self.out_scale)
+        self.ws = runtime.DecodeWorkspace(self.cfg, device)
+        self.flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.graph_step = self._capture(full=True)
+        self.graph_partial = self._capture(full=False)
+
+    def _bf16(self, a):
+        t = self.torch
+        a = np.ascontiguousarray(a, np.uint16)
+        return t.from_numpy(a.view(np.int16)).to(self.device, non_blocking=False).view(t.bfloat16)
+
+    def _cfg(self, out, out_scale):
+        w = self.w
+        return self.runtime.DecodeConfig(w.B, w.Hq, w.Dqk, w.Dv, getattr(self, "splits", 1),
+                                         w.Lmax, w.sm_scale, w.prob_scale, out, out_scale)
+
+    def _launch(self, full: bool, stream):
+        kvq = self.kvq
+        c = self.cache.struct()
+        p = self.cfg.params(self.seq_lens)
+        if full:
+            kvq.check(kvq.kvq_quantize_append(c, self.k_new, self.v_new, self.kpe_new,
+                                              self.start_pos, self.w.B, 1, stream))
+        kvq.check(kvq.kvq_decode_partial(c, p, self.q, self.ws.part_o, self.ws.part_lse, stream))
+        if full:
+            kvq.check(kvq.kvq_decode_combine(p, self.ws.part_o, self.ws.part_lse, self.ws.out,
+                                             stream))
+
+    def _capture(self, full: bool):
+        t = self.torch
+        with t.cuda.stream(self.stream):
+            self._launch(full, self.stream)     # warm (sets kernel attributes)
+        self.stream.synchronize()
+        g = t.cuda.CUDAGraph()
+        with t.cuda.graph(g, stream=self.stream):
+            self._launch(full, t.cuda.current_stream())
+        return g
+
+    def time_graph(self, g, steps: int, warmup: int):
+        t = self.torch
+        times = []
+        with t.cuda.stream(self.stream):
+            for i in range(warmup + steps):
+                self.flush.fill_(float(i))
+                e0 = t.cuda.Event(enable_timing=True)
+                e1 = t.cuda.Event(enable_timing=True)
+                e0.record(self.stream)
+                g.replay()
+                e1.record(self.stream)
+                if i >= warmup:
+                    times.append((e0, e1))
+        self.stream.synchronize()
+        return [a.elapsed_time(b) * 1e3 for a, b in times]   # microseconds
+
+    def e2e(self, steps: int, warmup: int):
+        """Through the public API with host buffers: pinned H2D of the step's
+        q and new K/V rows, append + partial + combine, D2H of the output."""
+        t = self.torch
+        pin = lambda x: x.cpu().pin_memory() if x is not None else None
+        hq, hk, hv, hkpe = pin(self.q), pin(self.k_new), pin(self.v_new), pin(self.kpe_new)
+        hout = t.empty(self.ws.out.shape, dtype=self.ws.out.dtype).pin_memory()
+        bi = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hkpe) if x is not None)
+        bo = hout.numel() * hout.element_size()
+        times = []
+        with t.cuda.stream(self.stream):
+            for i in range(warmup + steps):
+                self.flush.fill_(float(i))
+                e0 = t.cuda.Event(enable_timing=True)
+                e1 = t.cuda.Event(enable_timing=True)
+                e0.record(self.stream)
+                self.q.copy_(hq, non_blocking=True)
+                self.k_new.copy_(hk, non_blocking=True)
+                if hv is not None:
+                    self.v_new.copy_(hv, non_blocking=True)
+                if hkpe is not None:
+                    self.kpe_new.copy_(hkpe, non_blocking=True)
+                self._launch(True, self.stream)
+                hout.copy_(self.ws.out, non_blocking=True)
+                e1.record(self.stream)
+                e1.synchronize()
+                if i >= warmup:
+                    times.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.mean(times), bi, bo
+
+    def kv_bytes(self) -> int:
+        """Attended cache bytes per step: codes (+ block scales, + rope keys)."""
+        w = self.w
+        tok = int(np.sum(w.seq_lens))
+        if w.mla:
+            per = w.D // 2 + w.D // 16 + 2 * w.rope
+        else:
+            row = w.D if w.fmt == "fp8" else w.D // 2 + w.D // 16
+            per = 2 * w.Hkv * row
+        return tok * per
+
+    def partial_bytes(self) -> int:
+        """Algorithmic bytes of one partial launch: attended cache bytes,
+        block-table entries, Q, and the partial outputs written."""
+        w = self.w
+        ps = w.page_size_eff()
+        bt = int(sum(-(-int(L) // ps) for L in w.seq_lens)) * 4 * (1 if w.mla else w.Hkv)
+        q = w.B * w.Hq * w.Dqk * 2
+        parts = w.B * w.Hq * self.splits * (w.Dv + 1) * 4
+        return self.kv_bytes() + bt + q + parts
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from quantized_kv_cache_05_gb300 import synth
+
+    rank, world = env_int("RANK", 0), env_int("WORLD_SIZE", 1)
+    local = env_int("LOCAL_RANK", 0)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    w = synth.gqa_fp8(args.kv_len)
+    bench = Bench(w, device)
+    peak, peak_kind = hbm_peak()
+
+    # --- timed region: K graph replays of the whole step
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        step_us = bench.time_graph(bench.graph_step, args.steps, args.warmup)
+        part_us = bench.time_graph(bench.graph_partial, args.steps, args.warmup)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    us = statistics.mean(step_us)
+    if world > 1:
+        t = torch.tensor([us], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        us = float(t.item())
+    e2e_us, bi, bo = bench.e2e(max(10, args.steps // 2), args.warmup)
+    part = statistics.mean(part_us)
+    achieved = bench.partial_bytes() / (part * 1e-6) / 1e9
+    traffic = ncu_traffic(f"gqa_fp8_L{args.kv_len}")
+    kvb = bench.kv_bytes()
+    line = {
+        "metric": METRIC,
+        "value": round(us, 3),
+        "unit": "us/step",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(us / 1e3, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8_e4m3 KV codes -> f16 mma.sync, f32 accumulate",
+        "data": "synthetic (seeded bf16 N(0,1), 1% x10 outliers)",
+        "config": {
+            "workload": f"gqa_fp8: batch 2, Hq 32, Hkv 8, head_dim 128, kv_len {args.kv_len}, "
+                        f"FP8 E4M3 per-tensor KV, bf16 out, s=auto",
+            "batch": w.B, "kv_len": args.kv_len, "splits": bench.splits,
+            "step": "append 1 token + split-KV partial + combine (one CUDA graph)",
+            "l2": "flushed before every timed step (256 MiB write)",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "kv_bytes_per_step": kvb,
+        "kv_gbs": round(kvb / (us * 1e-6) / 1e9, 1),
+        "kv_hbm_frac": round(kvb / (us * 1e-6) / 1e9 / peak, 4),
+        "partial_us": round(part, 3),
+        "roofline": {
+            "kernel": "partial_kernel<FP8,128>",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "algorithmic_bytes_per_launch": bench.partial_bytes(),
+            "traffic": traffic,
+        },
+        "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo},
+        "gpu_launches": 3 * args.steps + args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_sweep:
+        line["sweep"] = sweep(device, args)
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(w, bench, seconds=args.cpu_seconds)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def sweep(device, args):
+    """Partial + combine (+ append) per workload, kv_len and split count."""
+    from quantized_kv_cache_05_gb300 import synth
+    peak, _ = hbm_peak()
+    res = []
+    plans = [("gqa_fp8", synth.gqa_fp8, [1024, 8192, 32768], [1, 2, 4, 8, 0]),
+             ("nvfp4", synth.nvfp4, [2048, 8192, 32768], [1, 2, 4, 8, 0]),
+             ("paged_fp8_probs", lambda L: synth.paged_fp8_probs(), [0], [1, 2, 0])]
+    for name, mk, lens, splits in plans:
+        for L in lens:
+            w = mk(L) if L else mk(None)
+            base = None
+            for s in splits:
+                try:
+                    b = Bench(w, device, splits=s) if base is None else base.with_splits(s)
+                except Exception as e:   # unsupported split for this workload
+                    res.append({"workload": name, "kv_len": L, "s": s, "error": str(e)[:120]})
+                    continue
+                base = base or b
+                st = b.time_graph(b.graph_step, args.sweep_steps, 3)
+                us = statistics.mean(st)
+                kvb = b.kv_bytes()
+                res.append({"workload": name, "kv_len": L or int(w.Lmax), "s": s or "auto",
+                            "splits": b.splits, "us_per_step": round(us, 2),
+                            "kv_gbs": round(kvb / (us * 1e-6) / 1e9, 1),
+                            "kv_hbm_frac": round(kvb / (us * 1e-6) / 1e9 / peak, 3)})
+            del base
+    return res
+
+
+def _with_splits(self, s):
+    import copy
+    nb = copy.copy(self)
+    nb.splits = s or self.runtime.auto_splits(self.w.B, self.w.Hkv, self.w.G, self.w.Lmax,
+                                              self.w.fmt, self.device)
+    nb.cfg = nb._cfg(self.w.out, self.out_scale)
+    nb.ws = self.runtime.DecodeWorkspace(nb.cfg, self.device)
+    nb.graph_step = nb._capture(full=True)
+    nb.graph_partial = None
+    return nb
+
+
+Bench.with_splits = _with_splits
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_step_time(w, groups, nthreads):
+    """Seconds for the oracle's decode step on the given (request, kv head)
+    groups: dequantize the group's cached codes and run exact attention for
+    its query heads.  Quantization of the cache is setup, not timed."""
+    import concurrent.futures
+    import oracle
+    from quantized_kv_cache_05_gb300 import synth
+
+    q = synth.bf16_to_f32(w.q()).astype(np.float64)
+    amax_k = max(oracle.amax_bf16(w.kv_rows(synth.T_K, b)) for b in range(w.B))
+    amax_v = max(oracle.amax_bf16(w.kv_rows(synth.T_V, b)) for b in range(w.B))
+    ks, vs = oracle.fp8_tensor_scale(amax_k), oracle.fp8_tensor_scale(amax_v)
+    codes = {}
+    for b, h in groups:
+        codes[(b, h)] = (oracle.fp8_quantize(w.kv_rows(synth.T_K, b)[:, h], ks),
+                         oracle.fp8_quantize(w.kv_rows(synth.T_V, b)[:, h], vs))
+
+    def one(bh):
+        b, h = bh
+        kc, vc = codes[bh]
+        kh = oracle.fp8_dequant(kc, ks)
+        vh = oracle.fp8_dequant(vc, vs)
+        qs = q[b, h * w.G:(h + 1) * w.G][None]
+        oracle.decode_batch(qs, kh[None, None], vh[None, None], np.array([kh.shape[0]]),
+                            w.sm_scale, nthreads=1)
+
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(nthreads) as ex:
+        list(ex.map(one, groups))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, bench=None, seconds=10.0):
+    nthreads = os.cpu_count() or 1
+    all_groups = [(b, h) for b in range(w.B) for h in range(w.Hkv)]
+    # size the sample: time one group, then take as many as fit the budget
+    t1 = oracle_step_time(w, all_groups[:1], 1)
+    n = int(max(1, min(len(all_groups), seconds / max(t1, 1e-6) * nthreads / 2)))
+    sample = all_groups[:n]
+    reps, tot = 0, 0.0
+    while tot < seconds / 2 and reps < 50:
+        tot += oracle_step_time(w, sample, nthreads)
+        reps += 1
+    per_step = tot / reps * len(all_groups) / len(sample)
+    return {"value": round(per_step * 1e6, 1), "unit": "us/step", "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"{len(sample)} of {len(all_groups)} (request, kv head) groups, "
+                      f"{reps} repetitions, scaled to the whole step"}
+
+
+def run_reference(args):
+    from quantized_kv_cache_05_gb300 import synth
+    rank = env_int("RANK", 0)
+    if rank != 0:
+        return
+    w = synth.gqa_fp8(args.kv_len)
+    nthreads = os.cpu_count() or 1
+    groups = [(b, h) for b in range(w.B) for h in range(w.Hkv)]
+    t1 = oracle_step_time(w, groups[:1], 1)
+    n = int(max(1, min(len(groups), 2.0 / max(t1, 1e-6) * nthreads / 2)))
+    sample = groups[:n]
+    for _ in range(args.warmup if args.warmup < 3 else 1):
+        oracle_step_time(w, sample, nthreads)
+    times = [oracle_step_time(w, sample, nthreads) * len(groups) / len(sample)
+             for _ in range(args.steps)]
+    us = statistics.mean(times) * 1e6
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(us, 1), "unit": "us/step", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded bf16 N(0,1), 1% x10 outliers)",
+        "config": {"workload": f"gqa_fp8: batch 2, Hq 32, Hkv 8, head_dim 128, kv_len "
+                               f"{args.kv_len}, FP8 E4M3 per-tensor KV", "batch": w.B,
+                   "kv_len": args.kv_len},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us/step", "cores": nthreads,
+                         "kind": "oracle",
+                         "sample": f"{len(sample)} of {len(groups)} (request, kv head) groups "
+                                   f"per step, scaled to the whole step"},
+        "e2e": {"value": round(us, 1), "unit": "us/step", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--kv-len", type=int, default=HEADLINE_L)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--sweep-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,225 @@
+/*
+ * kvq.h -- C ABI of the GB300 (sm_103a) library for attention decode over a
+ * quantized KV cache.
+ *
+ * What it computes (sources are the web pages the library follows):
+ *  - Quantize-on-append of new K/V rows into the cache, as FP8 E4M3 with a
+ *    static per-tensor scale (compressed-tensors PR 436, kv_cache_scheme:
+ *    8-bit float, symmetric, strategy "tensor", dynamic false, minmax
+ *    observer) or as NVFP4: E2M1 values in blocks of 16 along head_dim with a
+ *    dynamic E4M3 block scale and an fp32 global scale (Model-Optimizer PR
+ *    714, Testing: quantizers "(2, 1) bit ... block_sizes={-1: 16, 'type':
+ *    'dynamic', 'scale_bits': (4, 3)}" with a calibrated amax).
+ *  - Split-KV flash decode (Model-Optimizer PR 1832, notes under the latency
+ *    tables): each (request, kv head) sequence is cut into s contiguous
+ *    chunks; kvq_decode_partial runs one partial softmax (running max,
+ *    denominator, weighted V) per chunk and kvq_decode_combine merges the s
+ *    partials.  kvq_auto_splits picks s from the SM count and batch x heads.
+ *  - Options: GQA/MHA head groups, paged blocks, FP8-quantized softmax
+ *    probabilities with a prob scale and FP8 output with an out scale (vLLM
+ *    PR 15734), and the MLA latent-cache variant (Model-Optimizer PR 714:
+ *    kv_c_bmm_quantizer on the 512-wide latent cache, q_bmm_quantizer off).
+ *
+ * Conventions (all calls):
+ *  - Every device buffer (cache, queries, outputs, workspace) is allocated
+ *    and owned by the caller.  The library allocates no memory and keeps no
+ *    per-call state; calls are re-entrant.
+ *  - Pointers marked (device) must be device (or managed) memory of the
+ *    current CUDA device; pointers marked (host) are read on the host.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream).  No call synchronizes.
+ *  - Every call validates its arguments first and returns KVQ_ERR_INVALID or
+ *    KVQ_ERR_UNSUPPORTED without launching anything.  After launching it
+ *    returns KVQ_ERR_CUDA if the launch reported an error.
+ *  - bf16 tensors are raw IEEE bfloat16 bit patterns (uint16).
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int kvq_status;
+#define KVQ_OK 0
+#define KVQ_ERR_INVALID 1      /* bad pointer, size, scale or layout */
+#define KVQ_ERR_UNSUPPORTED 2  /* valid but not implemented (dims, format) */
+#define KVQ_ERR_WORKSPACE 3    /* a workspace or scratch area is too small */
+#define KVQ_ERR_CUDA 4         /* the CUDA runtime reported an error */
+
+/* Cache formats */
+#define KVQ_FP8_E4M3 1
+#define KVQ_NVFP4 2
+
+/* Output types of kvq_decode_combine */
+#define KVQ_OUT_F32 0
+#define KVQ_OUT_BF16 1
+#define KVQ_OUT_E4M3 2
+
+/* Bits that kernels OR into kvq_decode_params.error_flag */
+#define KVQ_DEVERR_WAIT_TIMEOUT 1   /* a pipeline wait gave up (results invalid) */
+#define KVQ_DEVERR_SEQ_CLAMPED 2    /* seq_lens[b] exceeded the cache; clamped */
+#define KVQ_DEVERR_BAD_PAGE 4       /* a block-table entry was out of range; page 0 read */
+
+/*
+ * A paged quantized KV cache.  Caller-owned plain struct; the library only
+ * reads it.
+ *
+ * Layout of one cache tensor (K or V), page-major then head-major, so one
+ * (page, kv head) is a contiguous run of page_size rows:
+ *   FP8:    codes  uint8 [num_pages][num_kv_heads][page_size][head_dim]
+ *   NVFP4:  codes  uint8 [num_pages][num_kv_heads][page_size][head_dim/2]
+ *                  (element 2i in the low nibble, 2i+1 in the high nibble)
+ *           bscale uint8 [num_pages][num_kv_heads][page_size][head_dim/16]
+ *                  (E4M3 block scales, one per 16 consecutive elements)
+ * Token t of request b lives in page block_table[b*max_pages_per_seq + t /
+ * page_size], row t % page_size.  A contiguous cache is the special case of
+ * one page per request (page_size = capacity, block_table[b][0] = b).
+ *
+ * Dequantized values: FP8 x = dec(code) * scale; NVFP4 x = dec(e2m1) *
+ * dec(bscale) * scale, where scale is k_scale or v_scale.
+ *
+ * MLA latent cache (rope_dim > 0): k_codes/k_bscale hold the NVFP4 latent
+ * kv_c (num_kv_heads = 1, head_dim = 512), k_pe holds the bf16 rope keys
+ * [num_pages][page_size][rope_dim], v_codes is NULL and v_is_k_latent = 1
+ * (the values are the latent itself).
+ */
+typedef struct kvq_cache {
+  int32_t fmt;               /* KVQ_FP8_E4M3 or KVQ_NVFP4 */
+  int32_t num_pages;         /* >= 1 */
+  int32_t page_size;         /* tokens per page, a multiple of 16 */
+  int32_t num_kv_heads;      /* Hkv >= 1 */
+  int32_t head_dim;          /* D: FP8 64 or 128; NVFP4 128 (MLA 512) */
+  void* k_codes;             /* (device) 16-byte aligned */
+  void* v_codes;             /* (device) 16-byte aligned; NULL for MLA */
+  void* k_bscale;            /* (device) NVFP4 only, 16-byte aligned */
+  void* v_bscale;            /* (device) NVFP4 only, 16-byte aligned */
+  float k_scale;             /* FP8 scale or NVFP4 global scale, finite > 0 */
+  float v_scale;             /* as k_scale (ignored for MLA) */
+  const int32_t* block_table;/* (device) [batch][max_pages_per_seq] */
+  int32_t max_pages_per_seq; /* >= 1 */
+  int32_t rope_dim;          /* MLA: 64; otherwise 0 */
+  void* k_pe;                /* (device) MLA only: bf16 rope keys */
+  int32_t v_is_k_latent;     /* MLA: 1; otherwise 0 */
+} kvq_cache;
+
+/* Parameters of one decode step (shared by partial and combine). */
+typedef struct kvq_decode_params {
+  int32_t batch;             /* B >= 0 (0 is a no-op) */
+  int32_t num_q_heads;       /* Hq, a multiple of Hkv; Hq/Hkv <= 16 */
+  int32_t qk_dim;            /* head_dim (MLA: 512 + 64 = 576) */
+  int32_t v_dim;             /* head_dim (MLA: 512) */
+  int32_t num_splits;        /* s >= 1 (see kvq_auto_splits) */
+  const int32_t* seq_lens;   /* (device) [batch] tokens per request */
+  int32_t max_kv_len;        /* (host) upper bound of seq_lens[] */
+  float sm_scale;            /* softmax scale (e.g. 1/sqrt(head_dim)) */
+  float prob_scale;          /* > 0: FP8 softmax probabilities; 0: off */
+  int32_t out_dtype;         /* KVQ_OUT_* (used by combine) */
+  float out_scale;           /* KVQ_OUT_E4M3: output scale, finite > 0 */
+  int32_t* error_flag;       /* (device, optional) KVQ_DEVERR_* bits OR-ed in */
+} kvq_decode_params;
+
+/* Human-readable name of a status code (static string). */
+const char* kvq_status_string(kvq_status s);
+
+/*
+ * Static per-tensor scale from a calibrated amax (the minmax observer of
+ * compressed-tensors PR 436; the MaxCalibrator amax of Model-Optimizer PR
+ * 714).  Host only.
+ *   KVQ_FP8_E4M3: scale = fl32(amax / 448)   (448 = largest E4M3 value)
+ *   KVQ_NVFP4:    scale = fl32(amax / 2688)  (2688 = 6 * 448: largest E2M1
+ *                 value times largest E4M3 block scale)
+ * amax == 0 gives 1.0.  Negative, NaN or infinite amax -> KVQ_ERR_INVALID.
+ */
+kvq_status kvq_tensor_scale(int fmt, float amax, float* scale_out /* host */);
+
+/*
+ * amax = max |x| over n bf16 values, written to *amax_out (device float).
+ * The calibration step that feeds kvq_tensor_scale.  n may be 0 (gives 0).
+ */
+kvq_status kvq_amax_bf16(const void* x /* device bf16 [n] */, size_t n,
+                         float* amax_out /* device */, void* stream);
+
+/*
+ * Quantize-on-append.  Writes n_tokens new rows per request into the cache:
+ * row t of request b goes to position start_pos[b] + t.
+ *   k_new   (device) bf16 [batch][n_tokens][num_kv_heads][head_dim]
+ *   v_new   (device) bf16, same shape (NULL for MLA)
+ *   kpe_new (device) bf16 [batch][n_tokens][rope_dim] (MLA only, else NULL)
+ *   start_pos (device) int32 [batch]
+ * FP8:   code = E4M3(fl32(x / scale)), round to nearest even, saturating at
+ *        +-448 (the sign of zero is kept).
+ * NVFP4, per 16-element block along head_dim:
+ *        bamax = max |x|;  sc = E4M3(fl32(fl32(bamax / 6) / scale));
+ *        es = fl32(dec(sc) * scale);  code = E2M1(fl32(x / es)) (all 0 when
+ *        es == 0), round to nearest even, saturating at +-6.
+ * The caller guarantees that the pages for positions start_pos[b] ..
+ * start_pos[b] + n_tokens - 1 exist in the block table; positions past
+ * max_pages_per_seq * page_size are skipped (not written).
+ * Input pointers must be 16-byte aligned.
+ */
+kvq_status kvq_quantize_append(const kvq_cache* c, const void* k_new, const void* v_new,
+                               const void* kpe_new, const int32_t* start_pos, int batch,
+                               int n_tokens, void* stream);
+
+/*
+ * Split-count heuristic (host only, deterministic).  base = batch *
+ * num_kv_heads (MLA: batch) CTAs per split.  s = ceil(2 * num_sms / base)
+ * (two CTAs per SM), then lowered so that every chunk keeps at least 256
+ * tokens, clamped to [1, 64].  num_sms is the device's multiprocessor count
+ * (cudaDevAttrMultiProcessorCount).  q_per_kv and fmt are accepted for
+ * future tuning and currently do not change the result.
+ */
+kvq_status kvq_auto_splits(int num_sms, int batch, int num_kv_heads, int q_per_kv,
+                           int max_kv_len, int fmt, int* out_s /* host */);
+
+/* Bytes of the split partials: part_o (fp32 [batch][Hq][s][v_dim]) plus
+ * part_lse (fp32 [batch][Hq][s]). */
+size_t kvq_partial_workspace_bytes(int batch, int num_q_heads, int num_splits, int v_dim);
+
+/*
+ * Split-KV partial.  For request b, query head hq (kv head hq / (Hq/Hkv))
+ * and split j, over chunk j of the request's sequence (chunk length c =
+ * ceil(L/s) rounded up to 16 tokens; chunk j = [j*c, min((j+1)*c, L))):
+ *   S_i = sm_scale * q . k^_i;   m = max_i S_i;   l = sum_i exp(S_i - m)
+ *   part_o[b][hq][j][:] = sum_i exp(S_i - m) v^_i / l
+ *   part_lse[b][hq][j]  = m + ln l          (-inf and o = 0 for empty chunks)
+ * With prob_scale > 0 (FP8 probabilities) the weight of v^_i is
+ *   p_q = dec(E4M3(fl32(p~ / prob_scale))) * prob_scale, p~ = exp(S_i - m)
+ * in fp32 with m the chunk max, while l sums the unquantized p~.
+ *   q (device) bf16 [batch][Hq][qk_dim], 16-byte aligned.
+ *   part_o, part_lse (device) as in kvq_partial_workspace_bytes.
+ * With prob_scale > 0 one chunk's scores must fit in on-chip memory:
+ * ceil(max_kv_len / s) rounded up to 16, times Hq/Hkv, at most 16384;
+ * larger chunks return KVQ_ERR_UNSUPPORTED (raise num_splits).
+ */
+kvq_status kvq_decode_partial(const kvq_cache* c, const kvq_decode_params* p, const void* q,
+                              float* part_o, float* part_lse, void* stream);
+
+/*
+ * Combine of the s partials of kvq_decode_partial:
+ *   M = max_j lse_j;  w_j = exp(lse_j - M);  O = sum_j w_j o_j / sum_j w_j
+ * (partials with lse = -inf are skipped; O = 0 when all are empty), written
+ * to out (device) [batch][Hq][v_dim] as fp32, bf16 (round to nearest even)
+ * or E4M3 codes E4M3(fl32(O / out_scale)) per p->out_dtype.
+ */
+kvq_status kvq_decode_combine(const kvq_decode_params* p, const float* part_o,
+                              const float* part_lse, void* out, void* stream);
+
+/*
+ * Elementwise fp32 -> code conversions with the device encoders the append
+ * path uses: out[i] = E4M3(x[i]) (round to nearest even, saturating at
+ * +-448) or the E2M1 nibble of x[i] (saturating at +-6) in the low 4 bits.
+ * x and out (device), n >= 0.  NaN inputs give unspecified codes.
+ */
+kvq_status kvq_encode_e4m3(const float* x, uint8_t* out, size_t n, void* stream);
+kvq_status kvq_encode_e2m1(const float* x, uint8_t* out, size_t n, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,287 @@
+// The extern "C" entry points of include/kvq.h: argument validation (before
+// any launch), TMA descriptor setup and kernel dispatch.  Host code only.
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "kvq.h"
+#include "kvq_internal.h"
+
+using namespace kvq;
+
+namespace {
+
+bool finite_pos(float x) { return std::isfinite(x) && x > 0.f; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  // The driver entry point is looked up once per process.
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D byte view [rows][row_bytes] of a cache tensor, 16-row boxes, with the
+// widest hardware swizzle the row allows.
+bool make_row_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)row_bytes, (cuuint32_t)kBoxTokens};
+  cuuint32_t estr[2] = {1, 1};
+  CUtensorMapSwizzle sw = row_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                            : CU_TENSOR_MAP_SWIZZLE_NONE;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool is_mla(const kvq_cache* c) { return c->rope_dim > 0; }
+
+// Checks shared by append and decode.
+kvq_status check_cache(const kvq_cache* c) {
+  if (!c) return KVQ_ERR_INVALID;
+  if (c->fmt != KVQ_FP8_E4M3 && c->fmt != KVQ_NVFP4) return KVQ_ERR_INVALID;
+  if (c->num_pages < 1 || c->num_kv_heads < 1 || c->max_pages_per_seq < 1) return KVQ_ERR_INVALID;
+  if (c->page_size < 16 || c->page_size % 16 != 0) return KVQ_ERR_INVALID;
+  if (c->head_dim < 16 || c->head_dim % 16 != 0 || c->head_dim > 1024) return KVQ_ERR_INVALID;
+  if ((long long)c->num_pages * c->num_kv_heads * c->page_size >= (1LL << 31))
+    return KVQ_ERR_UNSUPPORTED;
+  if (!c->block_table || !c->k_codes || !aligned16(c->k_codes)) return KVQ_ERR_INVALID;
+  if (!finite_pos(c->k_scale)) return KVQ_ERR_INVALID;
+  if (c->fmt == KVQ_NVFP4 && (!c->k_bscale || !aligned16(c->k_bscale))) return KVQ_ERR_INVALID;
+  if (is_mla(c)) {
+    if (c->rope_dim % 8 != 0 || !c->k_pe || !aligned16(c->k_pe)) return KVQ_ERR_INVALID;
+    if (c->v_codes || !c->v_is_k_latent) return KVQ_ERR_INVALID;
+    if (c->num_kv_heads != 1) return KVQ_ERR_INVALID;
+    if (c->fmt != KVQ_NVFP4) return KVQ_ERR_UNSUPPORTED;
+  } else {
+    if (c->rope_dim != 0 || c->k_pe || c->v_is_k_latent) return KVQ_ERR_INVALID;
+    if (!c->v_codes || !aligned16(c->v_codes) || !finite_pos(c->v_scale)) return KVQ_ERR_INVALID;
+    if (c->fmt == KVQ_NVFP4 && (!c->v_bscale || !aligned16(c->v_bscale))) return KVQ_ERR_INVALID;
+  }
+  return KVQ_OK;
+}
+
+kvq_status check_params(const kvq_decode_params* p) {
+  if (!p) return KVQ_ERR_INVALID;
+  if (p->batch < 0 || p->num_q_heads < 1 || p->qk_dim < 1 || p->v_dim < 1) return KVQ_ERR_INVALID;
+  if (p->num_splits < 1 || p->num_splits > 4096) return KVQ_ERR_INVALID;
+  if (p->max_kv_len < 0) return KVQ_ERR_INVALID;
+  if (p->batch > 0 && !p->seq_lens) return KVQ_ERR_INVALID;
+  if (!finite_pos(p->sm_scale)) return KVQ_ERR_INVALID;
+  if (!std::isfinite(p->prob_scale) || p->prob_scale < 0.f) return KVQ_ERR_INVALID;
+  if (p->out_dtype < KVQ_OUT_F32 || p->out_dtype > KVQ_OUT_E4M3) return KVQ_ERR_INVALID;
+  if (p->out_dtype == KVQ_OUT_E4M3 && !finite_pos(p->out_scale)) return KVQ_ERR_INVALID;
+  return KVQ_OK;
+}
+
+kvq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KVQ_ERR_WORKSPACE: return "workspace too small";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+kvq_status kvq_tensor_scale(int fmt, float amax, float* scale_out) {
+  if (!scale_out) return KVQ_ERR_INVALID;
+  if (!std::isfinite(amax) || amax < 0.f) return KVQ_ERR_INVALID;
+  float top;
+  if (fmt == KVQ_FP8_E4M3) top = 448.0f;
+  else if (fmt == KVQ_NVFP4) top = 2688.0f;
+  else return KVQ_ERR_INVALID;
+  *scale_out = amax == 0.f ? 1.0f : amax / top;   // one IEEE fp32 division
+  return KVQ_OK;
+}
+
+kvq_status kvq_amax_bf16(const void* x, size_t n, float* amax_out, void* stream) {
+  if (!amax_out || (n > 0 && !x)) return KVQ_ERR_INVALID;
+  return cuda_status(
+      launch_amax_bf16(static_cast<const uint16_t*>(x), n, amax_out, as_stream(stream)));
+}
+
+kvq_status kvq_encode_e4m3(const float* x, uint8_t* out, size_t n, void* stream) {
+  if (n > 0 && (!x || !out)) return KVQ_ERR_INVALID;
+  return cuda_status(launch_encode(0, x, out, n, as_stream(stream)));
+}
+
+kvq_status kvq_encode_e2m1(const float* x, uint8_t* out, size_t n, void* stream) {
+  if (n > 0 && (!x || !out)) return KVQ_ERR_INVALID;
+  return cuda_status(launch_encode(1, x, out, n, as_stream(stream)));
+}
+
+kvq_status kvq_quantize_append(const kvq_cache* c, const void* k_new, const void* v_new,
+                               const void* kpe_new, const int32_t* start_pos, int batch,
+                               int n_tokens, void* stream) {
+  kvq_status s = check_cache(c);
+  if (s != KVQ_OK) return s;
+  if (batch < 0 || n_tokens < 0) return KVQ_ERR_INVALID;
+  if (batch == 0 || n_tokens == 0) return KVQ_OK;
+  if (!k_new || !aligned16(k_new) || !start_pos) return KVQ_ERR_INVALID;
+  if (c->fmt == KVQ_FP8_E4M3 && c->head_dim % 8 != 0) return KVQ_ERR_INVALID;
+  if (is_mla(c)) {
+    if (v_new || !kpe_new || !aligned16(kpe_new)) return KVQ_ERR_INVALID;
+  } else {
+    if (!v_new || !aligned16(v_new) || kpe_new) return KVQ_ERR_INVALID;
+  }
+  if ((long long)batch * n_tokens * c->num_kv_heads * c->head_dim >= (1LL << 40))
+    return KVQ_ERR_UNSUPPORTED;
+  AppendArgs a{};
+  a.fmt = c->fmt;
+  a.D = c->head_dim;
+  a.Hkv = c->num_kv_heads;
+  a.ps = c->page_size;
+  a.max_pages = c->max_pages_per_seq;
+  a.num_pages = c->num_pages;
+  a.batch = batch;
+  a.T = n_tokens;
+  a.rope = is_mla(c) ? c->rope_dim : 0;
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.kpe_new = static_cast<const uint16_t*>(kpe_new);
+  a.start_pos = start_pos;
+  a.block_table = c->block_table;
+  a.k_codes = static_cast<uint8_t*>(c->k_codes);
+  a.v_codes = static_cast<uint8_t*>(c->v_codes);
+  a.k_bscale = static_cast<uint8_t*>(c->k_bscale);
+  a.v_bscale = static_cast<uint8_t*>(c->v_bscale);
+  a.k_pe = static_cast<uint16_t*>(c->k_pe);
+  a.k_scale = c->k_scale;
+  a.v_scale = c->v_scale;
+  a.has_v = is_mla(c) ? 0 : 1;
+  return cuda_status(launch_append(a, as_stream(stream)));
+}
+
+kvq_status kvq_auto_splits(int num_sms, int batch, int num_kv_heads, int q_per_kv,
+                           int max_kv_len, int fmt, int* out_s) {
+  (void)q_per_kv;
+  (void)fmt;
+  if (!out_s || num_sms < 1 || batch < 1 || num_kv_heads < 1 || max_kv_len < 0)
+    return KVQ_ERR_INVALID;
+  const long long base = (long long)batch * num_kv_heads;
+  long long s = (2LL * num_sms + base - 1) / base;
+  const long long by_len = max_kv_len / 256;
+  if (s > by_len) s = by_len;
+  if (s < 1) s = 1;
+  if (s > 64) s = 64;
+  *out_s = (int)s;
+  return KVQ_OK;
+}
+
+size_t kvq_partial_workspace_bytes(int batch, int num_q_heads, int num_splits, int v_dim) {
+  if (batch < 0 || num_q_heads < 0 || num_splits < 0 || v_dim < 0) return 0;
+  const size_t rows = (size_t)batch * num_q_heads * num_splits;
+  return rows * (size_t)v_dim * sizeof(float) + rows * sizeof(float);
+}
+
+kvq_status kvq_decode_partial(const kvq_cache* c, const kvq_decode_params* p, const void* q,
+                              float* part_o, float* part_lse, void* stream) {
+  kvq_status s = check_cache(c);
+  if (s != KVQ_OK) return s;
+  s = check_params(p);
+  if (s != KVQ_OK) return s;
+  if (p->batch == 0) return KVQ_OK;
+  if (!q || !aligned16(q) || !part_o || !part_lse) return KVQ_ERR_INVALID;
+  if (p->num_q_heads % c->num_kv_heads != 0) return KVQ_ERR_INVALID;
+  const int G = p->num_q_heads / c->num_kv_heads;
+  if (G > kMaxGroup) return KVQ_ERR_UNSUPPORTED;
+  if ((long long)p->max_kv_len > (long long)c->max_pages_per_seq * c->page_size)
+    return KVQ_ERR_INVALID;
+  if ((long long)p->batch * c->num_kv_heads >= (1LL << 31)) return KVQ_ERR_UNSUPPORTED;
+  const bool probq = p->prob_scale > 0.f;
+  if (probq) {
+    long long chunk = ((long long)p->max_kv_len + p->num_splits - 1) / p->num_splits;
+    chunk = (chunk + 15) / 16 * 16;
+    if (chunk * G > kScoreCapacity) return KVQ_ERR_UNSUPPORTED;
+  }
+  const int D = c->head_dim;
+  const uint64_t rows = (uint64_t)c->num_pages * c->num_kv_heads * c->page_size;
+
+  PartialArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.k_bscale = static_cast<const uint8_t*>(c->k_bscale);
+  a.v_bscale = static_cast<const uint8_t*>(c->v_bscale);
+  a.k_pe = static_cast<const uint16_t*>(c->k_pe);
+  a.block_table = c->block_table;
+  a.seq_lens = p->seq_lens;
+  a.part_o = part_o;
+  a.part_lse = part_lse;
+  a.error_flag = p->error_flag;
+  a.batch = p->batch;
+  a.Hq = p->num_q_heads;
+  a.Hkv = c->num_kv_heads;
+  a.G = G;
+  a.ps = c->page_size;
+  a.max_pages = c->max_pages_per_seq;
+  a.num_pages = c->num_pages;
+  a.num_splits = p->num_splits;
+  a.max_kv_len = p->max_kv_len;
+  a.qk_scale_log2 = p->sm_scale * c->k_scale * 1.4426950408889634f;
+  a.prob_scale = p->prob_scale;
+
+  if (is_mla(c)) {
+    if (D != 512 || c->rope_dim != 64 || G != 16 || p->qk_dim != 576 || p->v_dim != 512)
+      return KVQ_ERR_UNSUPPORTED;
+    if (probq) return KVQ_ERR_UNSUPPORTED;
+    a.out_mult = c->k_scale;   // the values are the latent itself
+    CUtensorMap tk;
+    if (!make_row_map(&tk, c->k_codes, D / 2, rows)) return KVQ_ERR_CUDA;
+    return cuda_status(launch_mla_partial(tk, a, as_stream(stream)));
+  }
+  if (p->qk_dim != D || p->v_dim != D) return KVQ_ERR_INVALID;
+  const bool ok_dims = (c->fmt == KVQ_FP8_E4M3 && (D == 64 || D == 128)) ||
+                       (c->fmt == KVQ_NVFP4 && D == 128);
+  if (!ok_dims) return KVQ_ERR_UNSUPPORTED;
+  a.out_mult = probq ? c->v_scale * p->prob_scale : c->v_scale;
+  const uint64_t row_bytes = c->fmt == KVQ_FP8_E4M3 ? D : D / 2;
+  CUtensorMap tk, tv;
+  if (!make_row_map(&tk, c->k_codes, row_bytes, rows) ||
+      !make_row_map(&tv, c->v_codes, row_bytes, rows))
+    return KVQ_ERR_CUDA;
+  return cuda_status(launch_partial(c->fmt, D, probq, tk, tv, a, as_stream(stream)));
+}
+
+kvq_status kvq_decode_combine(const kvq_decode_params* p, const float* part_o,
+                              const float* part_lse, void* out, void* stream) {
+  kvq_status s = check_params(p);
+  if (s != KVQ_OK) return s;
+  if (p->batch == 0) return KVQ_OK;
+  if (!part_o || !part_lse || !out) return KVQ_ERR_INVALID;
+  if ((long long)p->batch * p->num_q_heads >= (1LL << 31)) return KVQ_ERR_UNSUPPORTED;
+  CombineArgs a{};
+  a.part_o = part_o;
+  a.part_lse = part_lse;
+  a.out = out;
+  a.rows = p->batch * p->num_q_heads;
+  a.num_splits = p->num_splits;
+  a.Dv = p->v_dim;
+  a.out_dtype = p->out_dtype;
+  a.out_scale = p->out_scale;
+  return cuda_status(launch_combine(a, as_stream(stream)));
+}
+
+}  // extern "C"

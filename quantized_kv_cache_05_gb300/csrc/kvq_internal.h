@@ -1,0 +1,72 @@
+// Internal launcher interface between the C-ABI layer (kvq_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace kvq {
+
+constexpr int kFmtFp8 = 1;
+constexpr int kFmtNvfp4 = 2;
+
+// Decode pipeline geometry shared by host and device code.
+constexpr int kTileTokens = 64;   // tokens per pipeline stage
+constexpr int kBoxTokens = 16;    // rows per TMA box (one 16-token page)
+constexpr int kConsumerWarps = 4; // each consumes one 16-token box per stage
+constexpr int kDecodeThreads = 32 * (1 + kConsumerWarps);
+constexpr int kStages = 4;
+constexpr int kMaxGroup = 16;     // query heads per kv head (MMA M = 16)
+constexpr int kScoreCapacity = 16384;  // fp32 scores per CTA in FP8-prob mode
+
+struct AppendArgs {
+  int fmt, D, Hkv, ps, max_pages, batch, T, rope, num_pages;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const uint16_t* kpe_new;
+  const int32_t* start_pos;
+  const int32_t* block_table;
+  uint8_t* k_codes;
+  uint8_t* v_codes;
+  uint8_t* k_bscale;
+  uint8_t* v_bscale;
+  uint16_t* k_pe;
+  float k_scale, v_scale;
+  int has_v;
+};
+
+struct PartialArgs {
+  const uint16_t* q;          // [B][Hq][Dqk] bf16
+  const uint8_t* k_bscale;    // NVFP4 block scales (1-D bulk copies)
+  const uint8_t* v_bscale;
+  const uint16_t* k_pe;       // MLA rope keys
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  float* part_o;
+  float* part_lse;
+  int32_t* error_flag;
+  int batch, Hq, Hkv, G, ps, max_pages, num_splits, max_kv_len, num_pages;
+  float qk_scale_log2;        // sm_scale * k_scale * log2(e)
+  float out_mult;             // v_scale (times prob_scale with FP8 probabilities)
+  float prob_scale;           // > 0: FP8 probabilities
+};
+
+struct CombineArgs {
+  const float* part_o;
+  const float* part_lse;
+  void* out;
+  int rows, num_splits, Dv, out_dtype;
+  float out_scale;
+};
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t st);
+cudaError_t launch_amax_bf16(const uint16_t* x, size_t n, float* out, cudaStream_t st);
+cudaError_t launch_encode(int kind, const float* x, uint8_t* out, size_t n, cudaStream_t st);
+cudaError_t launch_partial(int fmt, int D, bool probq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const PartialArgs& a, cudaStream_t st);
+cudaError_t launch_mla_partial(const CUtensorMap& tk, const PartialArgs& a, cudaStream_t st);
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
+
+}  // namespace kvq

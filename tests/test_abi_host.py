@@ -1,0 +1,187 @@
+"""The C-ABI library loads, exports every symbol include/kvq.h declares, and
+validates arguments on the host (no GPU needed: every call here is rejected
+before any CUDA call, or is host-only)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+from quantized_kv_cache_05_gb300 import build as kbuild
+from quantized_kv_cache_05_gb300 import kvq
+
+
+@pytest.fixture(scope="module")
+def L():
+    kbuild.build()
+    return kvq.lib()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(kvq.SIGNATURES), "binding covers exactly the header"
+
+
+def test_status_strings(L):
+    assert kvq.status_string(0) == "ok"
+    assert "invalid" in kvq.status_string(1)
+    assert kvq.status_string(99) == "unknown status"
+
+
+def test_tensor_scale():
+    assert kvq.kvq_tensor_scale(kvq.KVQ_FP8_E4M3, 448.0) == (0, 1.0)
+    assert kvq.kvq_tensor_scale(kvq.KVQ_NVFP4, 2688.0) == (0, 1.0)
+    assert kvq.kvq_tensor_scale(kvq.KVQ_FP8_E4M3, 0.0) == (0, 1.0)
+    st, s = kvq.kvq_tensor_scale(kvq.KVQ_FP8_E4M3, 7.53125)
+    assert st == 0 and s == float(ctypes.c_float(7.53125 / 448.0).value) or s > 0
+    for bad in [-1.0, math.nan, math.inf]:
+        assert kvq.kvq_tensor_scale(kvq.KVQ_FP8_E4M3, bad)[0] == kvq.KVQ_ERR_INVALID
+    assert kvq.kvq_tensor_scale(7, 1.0)[0] == kvq.KVQ_ERR_INVALID
+
+
+def test_tensor_scale_matches_oracle(orc):
+    import numpy as np
+    for amax in [1e-3, 0.5, 3.0, 7.53125, 141.0, 1234.5, 3e4]:
+        a = float(np.float32(amax))
+        assert kvq.kvq_tensor_scale(kvq.KVQ_FP8_E4M3, a)[1] == orc.fp8_tensor_scale(a)
+        assert kvq.kvq_tensor_scale(kvq.KVQ_NVFP4, a)[1] == orc.nvfp4_global_scale(a)
+
+
+def test_auto_splits():
+    f = kvq.kvq_auto_splits
+    # 152 SMs, GQA 2 x 8 kv heads: ceil(304/16) = 19, long sequences keep it
+    assert f(152, 2, 8, 4, 32768, 1) == (0, 19)
+    assert f(152, 2, 8, 4, 8192, 1) == (0, 19)
+    # short sequences: at least 256 tokens per chunk
+    assert f(152, 2, 8, 4, 1024, 1) == (0, 4)
+    assert f(152, 2, 8, 4, 100, 1) == (0, 1)
+    # batch 1 x 8 kv heads: ceil(304/8) = 38
+    assert f(152, 1, 8, 4, 32768, 2) == (0, 38)
+    # large batch: one split
+    assert f(152, 64, 16, 1, 8192, 1) == (0, 1)
+    # clamp at 64
+    assert f(152, 1, 1, 16, 1 << 20, 2) == (0, 64)
+    assert f(0, 1, 1, 1, 10, 1)[0] == kvq.KVQ_ERR_INVALID
+    assert f(152, 0, 1, 1, 10, 1)[0] == kvq.KVQ_ERR_INVALID
+
+
+def test_workspace_bytes():
+    assert kvq.kvq_partial_workspace_bytes(2, 32, 8, 128) == 2 * 32 * 8 * (128 + 1) * 4
+    assert kvq.kvq_partial_workspace_bytes(-1, 1, 1, 1) == 0
+
+
+def good_cache():
+    c = kvq.kvq_cache()
+    c.fmt, c.num_pages, c.page_size, c.num_kv_heads, c.head_dim = 1, 4, 16, 2, 128
+    c.k_codes, c.v_codes = 0x10000, 0x20000
+    c.k_scale = c.v_scale = 0.5
+    c.block_table, c.max_pages_per_seq = 0x30000, 4
+    return c
+
+
+def good_params():
+    p = kvq.kvq_decode_params()
+    p.batch, p.num_q_heads, p.qk_dim, p.v_dim, p.num_splits = 1, 8, 128, 128, 2
+    p.seq_lens, p.max_kv_len, p.sm_scale = 0x40000, 64, 0.088
+    return p
+
+
+@pytest.mark.parametrize("mutate", [
+    lambda c, p: setattr(c, "fmt", 3),
+    lambda c, p: setattr(c, "page_size", 24),
+    lambda c, p: setattr(c, "page_size", 0),
+    lambda c, p: setattr(c, "num_pages", 0),
+    lambda c, p: setattr(c, "k_codes", None),
+    lambda c, p: setattr(c, "k_codes", 0x10008),        # not 16-byte aligned
+    lambda c, p: setattr(c, "v_codes", None),
+    lambda c, p: setattr(c, "k_scale", math.nan),
+    lambda c, p: setattr(c, "v_scale", 0.0),
+    lambda c, p: setattr(c, "k_scale", -1.0),
+    lambda c, p: setattr(c, "block_table", None),
+    lambda c, p: setattr(p, "num_splits", 0),
+    lambda c, p: setattr(p, "num_q_heads", 7),          # not a multiple of Hkv
+    lambda c, p: setattr(p, "sm_scale", math.inf),
+    lambda c, p: setattr(p, "prob_scale", -0.5),
+    lambda c, p: setattr(p, "max_kv_len", 65),          # beyond 4 pages x 16
+    lambda c, p: setattr(p, "seq_lens", None),
+    lambda c, p: setattr(p, "qk_dim", 64),
+    lambda c, p: (setattr(c, "fmt", 2)),                 # NVFP4 without block scales
+], ids=lambda f: "case")
+def test_decode_partial_rejects_without_launch(L, mutate):
+    c, p = good_cache(), good_params()
+    mutate(c, p)
+    st = kvq.kvq_decode_partial(c, p, 0x50000, 0x60000, 0x70000, None)
+    assert st in (kvq.KVQ_ERR_INVALID, kvq.KVQ_ERR_UNSUPPORTED)
+
+
+@pytest.mark.parametrize("mutate,want", [
+    (lambda c, p: (setattr(c, "head_dim", 96), setattr(p, "qk_dim", 96), setattr(p, "v_dim", 96)),
+     kvq.KVQ_ERR_UNSUPPORTED),
+    (lambda c, p: setattr(p, "num_q_heads", 64), kvq.KVQ_ERR_UNSUPPORTED),   # G = 32
+    (lambda c, p: (setattr(p, "prob_scale", 1 / 448), setattr(p, "num_splits", 1),
+                   setattr(c, "max_pages_per_seq", 2000), setattr(p, "max_kv_len", 20000)),
+     kvq.KVQ_ERR_UNSUPPORTED),                                               # scores too big
+])
+def test_decode_partial_unsupported(L, mutate, want):
+    c, p = good_cache(), good_params()
+    mutate(c, p)
+    assert kvq.kvq_decode_partial(c, p, 0x50000, 0x60000, 0x70000, None) == want
+
+
+def test_decode_null_outputs(L):
+    c, p = good_cache(), good_params()
+    assert kvq.kvq_decode_partial(c, p, None, 0x60000, 0x70000, None) == kvq.KVQ_ERR_INVALID
+    assert kvq.kvq_decode_partial(c, p, 0x50008, 0x60000, 0x70000, None) == kvq.KVQ_ERR_INVALID
+    assert kvq.kvq_decode_partial(None, p, 0x50000, 0x60000, 0x70000, None) == kvq.KVQ_ERR_INVALID
+    assert kvq.kvq_decode_partial(c, None, 0x50000, 0x60000, 0x70000, None) == kvq.KVQ_ERR_INVALID
+
+
+def test_decode_batch_zero_is_noop(L):
+    c, p = good_cache(), good_params()
+    p.batch = 0
+    assert kvq.kvq_decode_partial(c, p, None, None, None, None) == kvq.KVQ_OK
+    assert kvq.kvq_decode_combine(p, None, None, None, None) == kvq.KVQ_OK
+
+
+def test_combine_rejects(L):
+    p = good_params()
+    assert kvq.kvq_decode_combine(p, None, 0x1000, 0x2000, None) == kvq.KVQ_ERR_INVALID
+    p.out_dtype = 5
+    assert kvq.kvq_decode_combine(p, 0x1000, 0x1000, 0x2000, None) == kvq.KVQ_ERR_INVALID
+    p.out_dtype = kvq.KVQ_OUT_E4M3
+    p.out_scale = 0.0
+    assert kvq.kvq_decode_combine(p, 0x1000, 0x1000, 0x2000, None) == kvq.KVQ_ERR_INVALID
+
+
+def test_append_rejects(L):
+    c = good_cache()
+    f = kvq.kvq_quantize_append
+    assert f(c, None, 0x2000, None, 0x3000, 1, 1, None) == kvq.KVQ_ERR_INVALID
+    assert f(c, 0x1000, None, None, 0x3000, 1, 1, None) == kvq.KVQ_ERR_INVALID
+    assert f(c, 0x1000, 0x2000, 0x4000, 0x3000, 1, 1, None) == kvq.KVQ_ERR_INVALID  # kpe w/o MLA
+    assert f(c, 0x1000, 0x2000, None, None, 1, 1, None) == kvq.KVQ_ERR_INVALID
+    assert f(c, 0x1008, 0x2000, None, 0x3000, 1, 1, None) == kvq.KVQ_ERR_INVALID
+    assert f(c, 0x1000, 0x2000, None, 0x3000, -1, 1, None) == kvq.KVQ_ERR_INVALID
+    assert f(c, 0x1000, 0x2000, None, 0x3000, 0, 1, None) == kvq.KVQ_OK
+    assert f(c, 0x1000, 0x2000, None, 0x3000, 1, 0, None) == kvq.KVQ_OK
+    c.rope_dim = 64          # MLA needs k_pe, v_codes NULL, Hkv 1, NVFP4
+    assert f(c, 0x1000, None, 0x4000, 0x3000, 1, 1, None) == kvq.KVQ_ERR_INVALID
+
+
+def test_misc_rejects(L):
+    assert kvq.kvq_amax_bf16(None, 10, 0x1000, None) == kvq.KVQ_ERR_INVALID
+    assert kvq.kvq_amax_bf16(0x1000, 10, None, None) == kvq.KVQ_ERR_INVALID
+    assert kvq.kvq_encode_e4m3(None, 0x1000, 4, None) == kvq.KVQ_ERR_INVALID
+    assert kvq.kvq_encode_e2m1(0x1000, None, 4, None) == kvq.KVQ_ERR_INVALID
+    assert kvq.kvq_encode_e4m3(None, None, 0, None) == kvq.KVQ_OK

@@ -1,0 +1,167 @@
+"""GPU split-KV decode vs the oracle on the same dequantized cache.
+
+Sizes span several pipeline stages and ragged tails; every split count of
+the workloads plus uneven ones; partials checked chunk by chunk; edge cases:
+empty sequences, one token, fewer tokens than splits, constant keys."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kvq_testlib import (Setup, assert_bf16_close, assert_e4m3_close, assert_f32_close,
+                         bf16_bits)
+from quantized_kv_cache_05_gb300 import build as kbuild
+from quantized_kv_cache_05_gb300 import kvq, runtime, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    kbuild.build()
+    kvq.lib()
+    torch.cuda.init()
+
+
+def splits_of(w, s):
+    if s == 0:
+        return runtime.auto_splits(w.B, w.Hkv, w.G, w.Lmax, w.fmt)
+    return s
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return Setup(synth.tiny_fp8())
+
+
+@pytest.mark.parametrize("s", [1, 2])
+def test_tiny_fp8(tiny, s):
+    ref, _ = tiny.oracle_decode()
+    out, _ = tiny.gpu_decode(s)
+    assert_f32_close(out.cpu().numpy(), ref, f"tiny s={s}")
+
+
+@pytest.fixture(scope="module")
+def gqa():
+    return Setup(synth.gqa_fp8(1000))
+
+
+@pytest.mark.parametrize("s", [1, 2, 3, 4, 8, 0])
+def test_gqa_fp8_f32(gqa, s):
+    ref, _ = gqa.oracle_decode()
+    out, _ = gqa.gpu_decode(splits_of(gqa.w, s))
+    assert_f32_close(out.cpu().numpy(), ref, f"gqa s={s}")
+
+
+@pytest.mark.parametrize("s", [1, 8, 0])
+def test_gqa_fp8_bf16_out(gqa, s):
+    ref, _ = gqa.oracle_decode()
+    out, _ = gqa.gpu_decode(splits_of(gqa.w, s), "bf16")
+    assert_bf16_close(bf16_bits(out), ref, f"gqa bf16 s={s}")
+
+
+def test_gqa_partials_per_chunk(gqa):
+    s = 3
+    w = gqa.w
+    _, ws = gqa.gpu_decode(s)
+    po = ws.part_o.cpu().numpy().reshape(w.B, w.Hq, s, w.Dv)
+    pl = ws.part_lse.cpu().numpy().reshape(w.B, w.Hq, s)
+    q = gqa.q64()
+    for b in range(w.B):
+        for kvh in (0, w.Hkv - 1):
+            kh, vh = gqa.oracle_kv(b, kvh)
+            L = int(w.seq_lens[b])
+            for j in range(s):
+                st, en = oracle.chunk(L, s, j)
+                for hq in range(kvh * w.G, (kvh + 1) * w.G):
+                    o, l = oracle.attention_partial(q[b, hq], kh, vh, st, en, w.sm_scale)
+                    assert abs(pl[b, hq, j] - l) <= 1e-4 * max(1.0, abs(l)), (b, hq, j)
+                    assert_f32_close(po[b, hq, j], o, f"partial b{b} h{hq} j{j}")
+
+
+@pytest.fixture(scope="module")
+def nv():
+    return Setup(synth.nvfp4(1500))
+
+
+@pytest.mark.parametrize("s", [1, 4, 7, 0])
+def test_nvfp4(nv, s):
+    ref, _ = nv.oracle_decode()
+    out, _ = nv.gpu_decode(splits_of(nv.w, s))
+    assert_f32_close(out.cpu().numpy(), ref, f"nvfp4 s={s}")
+
+
+@pytest.fixture(scope="module")
+def paged():
+    return Setup(synth.paged_fp8_probs(B=6, lo=1, hi=700, seed=5))
+
+
+@pytest.mark.parametrize("s", [1, 2, 5])
+def test_paged_fp8_probs_f32(paged, s):
+    ref, _ = paged.oracle_decode(mode=1, s=s)
+    out, _ = paged.gpu_decode(s)
+    assert_f32_close(out.cpu().numpy(), ref, f"paged probs s={s}")
+
+
+@pytest.mark.parametrize("s", [1, 2])
+def test_paged_fp8_probs_e4m3_out(paged, s):
+    ref, _ = paged.oracle_decode(mode=1, s=s)
+    out_scale = float(np.float32(np.float32(np.max(np.abs(ref))) / np.float32(448.0)))
+    out, _ = paged.gpu_decode(s, "e4m3", out_scale)
+    flips = assert_e4m3_close(out.cpu().numpy(), ref, out_scale, f"paged e4m3 s={s}")
+    assert flips <= max(2, ref.size // 1000)
+
+
+def test_paged_exact_probabilities_off():
+    """The same paged MHA cache without FP8 probabilities matches exact
+    attention."""
+    w = synth.paged_fp8_probs(B=4, lo=17, hi=400, seed=9)
+    w.prob_fp8 = False
+    S = Setup(w)
+    ref, _ = S.oracle_decode()
+    out, _ = S.gpu_decode(2)
+    assert_f32_close(out.cpu().numpy(), ref, "paged exact")
+
+
+def test_edge_lengths():
+    """Lengths 0 (output 0), 1, 15, 16, 17 and fewer tokens than splits."""
+    w = synth.gqa_fp8(64)
+    w.seq_lens = np.array([0, 1, 15, 16, 17, 40], np.int32)
+    w.B = 6
+    w.page_size = 16
+    S = Setup(w)
+    ref, _ = S.oracle_decode()
+    for s in (1, 3, 8):
+        out, ws = S.gpu_decode(s)
+        o = out.cpu().numpy()
+        assert np.all(o[0] == 0)
+        assert_f32_close(o, ref, f"edge s={s}")
+        lse = ws.part_lse.cpu().numpy().reshape(w.B, w.Hq, s)
+        assert np.all(np.isneginf(lse[0]))
+
+
+def test_constant_keys_mean_values():
+    """All keys equal: the output is the mean of the dequantized values."""
+    w = synth.gqa_fp8(300)
+    w.B = 1
+    w.seq_lens = np.array([300], np.int32)
+    S = Setup.__new__(Setup)
+    Setup.__init__(S, w)
+    # overwrite the cache's K codes with one row repeated
+    kc = S.cache.k_codes
+    kc[:] = kc[:, :, :1, :].clone() if kc.shape[2] > 0 else kc
+    torch.cuda.synchronize()
+    out, _ = S.gpu_decode(2)
+    o = out.cpu().numpy()[0]
+    for kvh in range(w.Hkv):
+        vh = S.oracle_dequant("v", 0, kvh)
+        mean = vh.mean(axis=0)
+        for hq in range(kvh * w.G, (kvh + 1) * w.G):
+            assert np.max(np.abs(o[hq] - mean)) <= 2e-3
+
+
+def test_no_error_flag_and_repeatable(gqa):
+    a, _ = gqa.gpu_decode(4)
+    a = a.clone()
+    b, _ = gqa.gpu_decode(4)
+    assert torch.equal(a, b)
