@@ -8,10 +8,11 @@ tokens per request that is resident in HBM.  The headline workload is GQA
 elements x10, bf16 output.
 
 Timing: W warm-up steps, then K timed steps; before every timed step the L2
-is flushed by writing a 256 MiB buffer, and each step is bracketed by CUDA
-events on the launch stream (the three launches are replayed as one CUDA
-graph).  `value` is the mean device time per step in microseconds (lower is
-better); KV GB/s = attended cache bytes / step time.
+is flushed by writing one 256 MiB buffer and then reading another (the read
+evicts the written lines, so the timed step neither finds its data in L2 nor
+pays for write-backs of the flush), and each step is bracketed by CUDA events
+on the launch stream (the three launches are replayed as one CUDA graph).
+`value` is the mean device time per step in microseconds (lower is better); KV GB/s = attended cache bytes / step time.
 
     python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
                     [--no-sweep]
@@ -212,6 +213,8 @@ class Bench:
         self.cfg = self._cfg(w.out, self.out_scale)
         self.ws = runtime.DecodeWorkspace(self.cfg, device)
         self.flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.flush_rd = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.flush_sink = torch.zeros(1, dtype=torch.float32, device=device)
         self.graph_step = self._capture(full=True)
         self.graph_partial = self._capture(full=False)
 
@@ -247,12 +250,19 @@ class Bench:
             self._launch(full, t.cuda.current_stream())
         return g
 
+    def flush_l2(self, i: int):
+        """Evict L2: write a 256 MiB buffer, then read a second one so the
+        dirty lines are written back before the timed step."""
+        self.flush.fill_(float(i))
+        torch = self.torch
+        torch.sum(self.flush_rd, dim=0, keepdim=True, out=self.flush_sink)
+
     def time_graph(self, g, steps: int, warmup: int):
         t = self.torch
         times = []
         with t.cuda.stream(self.stream):
             for i in range(warmup + steps):
-                self.flush.fill_(float(i))
+                self.flush_l2(i)
                 e0 = t.cuda.Event(enable_timing=True)
                 e1 = t.cuda.Event(enable_timing=True)
                 e0.record(self.stream)
@@ -275,7 +285,7 @@ class Bench:
         times = []
         with t.cuda.stream(self.stream):
             for i in range(warmup + steps):
-                self.flush.fill_(float(i))
+                self.flush_l2(i)
                 e0 = t.cuda.Event(enable_timing=True)
                 e1 = t.cuda.Event(enable_timing=True)
                 e0.record(self.stream)
@@ -367,7 +377,7 @@ def run_ours(args):
                         f"FP8 E4M3 per-tensor KV, bf16 out, s=auto",
             "batch": w.B, "kv_len": args.kv_len, "splits": bench.splits,
             "step": "append 1 token + split-KV partial + combine (one CUDA graph)",
-            "l2": "flushed before every timed step (256 MiB write)",
+            "l2": "flushed before every timed step (256 MiB write, then 256 MiB read)",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "kv_bytes_per_step": kvb,

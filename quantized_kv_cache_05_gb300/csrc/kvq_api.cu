@@ -33,14 +33,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D byte view [rows][row_bytes] of a cache tensor, 16-row boxes, with the
+// 2-D byte view [rows][row_bytes] of a cache tensor, box_rows-row boxes, with the
 // widest hardware swizzle the row allows.
-bool make_row_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows) {
+bool make_row_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows,
+                  uint32_t box_rows = kBoxTokens) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {row_bytes, rows};
   cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {(cuuint32_t)row_bytes, (cuuint32_t)kBoxTokens};
+  cuuint32_t box[2] = {(cuuint32_t)row_bytes, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUtensorMapSwizzle sw = row_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
                           : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -182,12 +183,14 @@ kvq_status kvq_auto_splits(int num_sms, int batch, int num_kv_heads, int q_per_k
   (void)fmt;
   if (!out_s || num_sms < 1 || batch < 1 || num_kv_heads < 1 || max_kv_len < 0)
     return KVQ_ERR_INVALID;
+  // One wave of the partial kernel: kCtasPerSm resident CTAs on every SM.
+  constexpr long long kCtasPerSm = 3, kMinChunk = 128, kMaxSplits = 64;
   const long long base = (long long)batch * num_kv_heads;
-  long long s = (2LL * num_sms + base - 1) / base;
-  const long long by_len = max_kv_len / 256;
+  long long s = kCtasPerSm * num_sms / base;
+  const long long by_len = max_kv_len / kMinChunk;
   if (s > by_len) s = by_len;
   if (s < 1) s = 1;
-  if (s > 64) s = 64;
+  if (s > kMaxSplits) s = kMaxSplits;
   *out_s = (int)s;
   return KVQ_OK;
 }
@@ -258,11 +261,11 @@ kvq_status kvq_decode_partial(const kvq_cache* c, const kvq_decode_params* p, co
   if (!ok_dims) return KVQ_ERR_UNSUPPORTED;
   a.out_mult = probq ? c->v_scale * p->prob_scale : c->v_scale;
   const uint64_t row_bytes = c->fmt == KVQ_FP8_E4M3 ? D : D / 2;
-  CUtensorMap tk, tv;
-  if (!make_row_map(&tk, c->k_codes, row_bytes, rows) ||
-      !make_row_map(&tv, c->v_codes, row_bytes, rows))
+  TensorMaps maps;
+  if (!make_row_map(&maps.k16, c->k_codes, row_bytes, rows) ||
+      !make_row_map(&maps.v16, c->v_codes, row_bytes, rows))
     return KVQ_ERR_CUDA;
-  return cuda_status(launch_partial(c->fmt, D, probq, tk, tv, a, as_stream(stream)));
+  return cuda_status(launch_partial(c->fmt, D, probq, maps, a, as_stream(stream)));
 }
 
 kvq_status kvq_decode_combine(const kvq_decode_params* p, const float* part_o,

@@ -7,22 +7,33 @@
 // s partials.  FP8 probabilities and FP8 output follow vLLM PR 15734.
 //
 // GB300 design of the partial kernel
-//  * One producer warp streams the chunk's K/V code tiles HBM -> shared
-//    memory with TMA (cp.async.bulk.tensor, 16-row boxes = one 16-token page,
-//    hardware swizzle) into a 4-stage ring guarded by mbarriers; NVFP4 block
-//    scales come by 1-D bulk copies.
-//  * Four consumer warps each take one 16-token box per stage.  Codes are
-//    decoded in registers straight into tensor-core fragments (E4M3 -> f16 and
-//    E2M1 -> f16 with cvt, block scales by f16x2 multiply: all exact), and
-//    the scores Q.K^T and the update P.V run on mma.sync m16n8k16 with fp32
-//    accumulation.  The query heads of a group are the MMA's 16 rows.
+//  * Four warps per CTA, three CTAs per SM.  Each warp streams its own
+//    16-token boxes (box w, w+4, w+8, ... of the chunk) HBM -> shared memory
+//    with TMA (cp.async.bulk.tensor, 16-row box = one 16-token page,
+//    hardware swizzle; NVFP4 block scales by 1-D bulk copies) into a private
+//    4-deep ring with its own mbarriers, and consumes them itself: no
+//    producer warp, no cross-warp hand-off per box, and twelve warps per SM
+//    issuing copies (one issuing thread per CTA cannot keep HBM busy).  The
+//    chunk's block-table entries are cached in shared memory.
+//  * Codes are decoded in registers straight into tensor-core fragments
+//    (E4M3 -> f16 and E2M1 -> f16 with cvt, block scales by an f16x2
+//    multiply: all exact), and the contractions run on mma.sync m16n8k16 with
+//    fp32 accumulation:
+//      S^T = K Q^T     M = 16 tokens, N = 8 query heads, K = 16 head dims
+//      O^T = V^T P^T   M = 16 value dims, N = 8 query heads, K = 16 tokens
+//    P^T comes from the S^T accumulator by one movmatrix transpose per 8x8
+//    block, so every lane keeps the softmax state of the two heads its own
+//    accumulator columns hold (no shuffles on the common path).
 //  * Head-dim order inside a K row is permuted per lane so that each lane's
-//    codes come from one 16-byte shared-memory load; Q is loaded with the same
-//    permutation.  The token-pair layout the P.V fragment needs is built with
+//    codes come from 16-byte shared-memory loads; Q is loaded with the same
+//    permutation.  The token-pair layout of the V^T operand is built with
 //    byte permutes (FP8) or nibble masks (E2M1).
 //  * P is split into an f16 high part and an f16 residual (two MMAs), so the
 //    probabilities keep ~22 bits; with FP8 probabilities the E4M3 code itself
 //    is the (exact) f16 operand.
+//  * The running max moves only when a box's max exceeds it by more than
+//    2^8 (log2 domain), so O is rarely rescaled; the final normalization by
+//    the denominator is exact whatever the reference max.
 //  * Warps merge their (max, sum, O) states through shared memory at the end.
 // Every mbarrier wait is bounded; a timeout sets an error bit and the CTA
 // writes NaN for its partial instead of hanging.
@@ -37,18 +48,20 @@ namespace kvq {
 namespace {
 
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLazyMax = 8.0f;   // log2 headroom before the running max moves
 
 template <int FMT, int D>
 struct Geom {
   static constexpr int kRow = FMT == kFmtFp8 ? D : D / 2;   // code bytes per token row
   static constexpr int kSRow = FMT == kFmtFp8 ? 0 : D / 16; // scale bytes per token row
-  static constexpr int kTileK = kTileTokens * kRow;
-  static constexpr int kTileS = kTileTokens * kSRow;
-  static constexpr int kStage = 2 * (kTileK + kTileS);
-  static constexpr int kBoxK = kBoxTokens * kRow;
-  static constexpr int kBoxS = kBoxTokens * kSRow;
-  static constexpr int kKSteps = D / 16;                     // MMA k-steps over head_dim
-  static constexpr int kNT = D / 8;                          // n-tiles over v_dim
+  static constexpr int kBoxK = kBoxTokens * kRow;            // code bytes of one box
+  static constexpr int kBoxS = kBoxTokens * kSRow;           // scale bytes of one box
+  // one ring stage: [K codes][V codes][K scales][V scales], padded so that
+  // every stage starts on the 1024-byte swizzle period
+  static constexpr int kStage = (2 * (kBoxK + kBoxS) + 1023) / 1024 * 1024;
+  static constexpr int kRing = kDecodeWarps * kStages * kStage;
+  static constexpr int kKSteps = D / 16;   // QK k-steps over head_dim
+  static constexpr int kMT = D / 16;       // PV m-tiles over v_dim
   // physical 16-byte chunk of logical chunk `ch` in row `row` of a box
   __device__ static __forceinline__ int swz(int row, int ch) {
     if constexpr (kRow == 128) return ch ^ (row & 7);
@@ -57,13 +70,12 @@ struct Geom {
 };
 
 struct Smem {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kDecodeWarps][kStages];
   int abort_flag;
-  float m[kConsumerWarps][kMaxGroup];
-  float l[kConsumerWarps][kMaxGroup];
-  float fac[kConsumerWarps][kMaxGroup];
-  float lse[kMaxGroup];
+  int pages[kPageCache];
+  float m[kDecodeWarps][kMaxGroup];
+  float l[kDecodeWarps][kMaxGroup];
+  float fac[kDecodeWarps][kMaxGroup];
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
@@ -80,9 +92,9 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 }
 
 // ---------------------------------------------------------------------------
-// K fragments for one n-tile (8 tokens): b[j][0..1] for k-step j.
-// Lane (g, t) holds token row `row` (= 8u + g) and head-dim indices
-//   d = (D/4) * t + 4 j + {0, 1} (b[j][0]) and + {2, 3} (b[j][1]).
+// K fragments (B operand of S = Q K^T) for one 8-token n-tile: b[j][0..1] for
+// k-step j.  Lane (g, t) holds token row `row` (= 8u + g) and head dims
+//   d = (D/4) t + 4 j + {0, 1} (b[j][0]) and + {2, 3} (b[j][1]).
 // ---------------------------------------------------------------------------
 template <int FMT, int D>
 __device__ __forceinline__ void k_frag(uint32_t boxK, uint32_t boxKs, int row, int t,
@@ -93,12 +105,10 @@ __device__ __forceinline__ void k_frag(uint32_t boxK, uint32_t boxKs, int row, i
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
       uint4 v = lds128(boxK + row * Gm::kRow + (Gm::swz(row, t * NCH + i) << 4));
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        b[i * 4 + k][0] = e4m3x2_to_f16x2(w[k] & 0xFFFFu);
-        b[i * 4 + k][1] = e4m3x2_to_f16x2(w[k] >> 16);
-      }
+      e4m3x4_to_f16x2x2(v.x, b[i * 4 + 0][0], b[i * 4 + 0][1]);
+      e4m3x4_to_f16x2x2(v.y, b[i * 4 + 1][0], b[i * 4 + 1][1]);
+      e4m3x4_to_f16x2x2(v.z, b[i * 4 + 2][0], b[i * 4 + 2][1]);
+      e4m3x4_to_f16x2x2(v.w, b[i * 4 + 3][0], b[i * 4 + 3][1]);
     }
   } else {
     static_assert(D == 128, "NVFP4 decode supports head_dim 128");
@@ -121,72 +131,94 @@ __device__ __forceinline__ void k_frag(uint32_t boxK, uint32_t boxKs, int row, i
 }
 
 // ---------------------------------------------------------------------------
-// V fragments of a token pair (ta, tb) for all n-tiles: bv[j] = f16x2
-// (V[ta][d_j], V[tb][d_j]) with d_j = (D/8) * g + j for lane group g.
-// Invalid tokens read as zero codes.
+// V^T fragments (A operand of O^T = V^T P^T) for the box's 16 tokens:
+// a[i][0..3] for m-tile i.  Lane (g, t) covers tokens 2t, 2t+1 (a0, a1) and
+// 2t+8, 2t+9 (a2, a3); m-tile i, row g is value dim (D/8) g + 2 i and row
+// g + 8 is (D/8) g + 2 i + 1.  Invalid tokens read as zero codes.
 // ---------------------------------------------------------------------------
 template <int FMT, int D>
-__device__ __forceinline__ void v_pair(uint32_t boxV, uint32_t boxVs, int ta, int tb,
-                                       bool va, bool vb, int g, uint32_t (&bv)[D / 8]) {
+__device__ __forceinline__ void v_frag(uint32_t boxV, uint32_t boxVs, int t, int g, int nvalid,
+                                       uint32_t (&a)[D / 16][4]) {
   using Gm = Geom<FMT, D>;
-  if constexpr (FMT == kFmtFp8 && D == 128) {
-    uint4 A = lds128(boxV + ta * 128 + (Gm::swz(ta, g) << 4));
-    uint4 B = lds128(boxV + tb * 128 + (Gm::swz(tb, g) << 4));
-    if (!va) A = make_uint4(0, 0, 0, 0);
-    if (!vb) B = make_uint4(0, 0, 0, 0);
-    uint32_t a[4] = {A.x, A.y, A.z, A.w}, bb[4] = {B.x, B.y, B.z, B.w};
+  const int tk[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+  if constexpr (FMT == kFmtFp8) {
+    constexpr int NW = D / 32;   // words per lane per token (4 for D=128, 2 for D=64)
+    uint32_t w[4][NW];
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint32_t p0 = __byte_perm(a[w], bb[w], 0x5140);
-      uint32_t p1 = __byte_perm(a[w], bb[w], 0x7362);
-      bv[4 * w + 0] = e4m3x2_to_f16x2(p0 & 0xFFFFu);
-      bv[4 * w + 1] = e4m3x2_to_f16x2(p0 >> 16);
-      bv[4 * w + 2] = e4m3x2_to_f16x2(p1 & 0xFFFFu);
-      bv[4 * w + 3] = e4m3x2_to_f16x2(p1 >> 16);
+    for (int r = 0; r < 4; ++r) {
+      if constexpr (D == 128) {
+        uint4 v = lds128(boxV + tk[r] * 128 + (Gm::swz(tk[r], g) << 4));
+        w[r][0] = v.x; w[r][1] = v.y; w[r][2] = v.z; w[r][3] = v.w;
+      } else {
+        uint2 v = lds64(boxV + tk[r] * 64 + (Gm::swz(tk[r], g >> 1) << 4) + ((g & 1) << 3));
+        w[r][0] = v.x; w[r][1] = v.y;
+      }
+      if (tk[r] >= nvalid) {
+#pragma unroll
+        for (int k = 0; k < NW; ++k) w[r][k] = 0u;
+      }
     }
-  } else if constexpr (FMT == kFmtFp8 && D == 64) {
-    // 8 bytes per token: bytes [8g, 8g+8) = half (g & 1) of logical chunk g >> 1
-    uint2 A = lds64(boxV + ta * 64 + (Gm::swz(ta, g >> 1) << 4) + ((g & 1) << 3));
-    uint2 B = lds64(boxV + tb * 64 + (Gm::swz(tb, g >> 1) << 4) + ((g & 1) << 3));
-    if (!va) A = make_uint2(0, 0);
-    if (!vb) B = make_uint2(0, 0);
-    uint32_t a[2] = {A.x, A.y}, bb[2] = {B.x, B.y};
 #pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      uint32_t p0 = __byte_perm(a[w], bb[w], 0x5140);
-      uint32_t p1 = __byte_perm(a[w], bb[w], 0x7362);
-      bv[4 * w + 0] = e4m3x2_to_f16x2(p0 & 0xFFFFu);
-      bv[4 * w + 1] = e4m3x2_to_f16x2(p0 >> 16);
-      bv[4 * w + 2] = e4m3x2_to_f16x2(p1 & 0xFFFFu);
-      bv[4 * w + 3] = e4m3x2_to_f16x2(p1 >> 16);
+    for (int k = 0; k < NW; ++k) {
+      // token pairs (2t, 2t+1) and (2t+8, 2t+9), one byte of each per value dim
+      const uint32_t p0 = __byte_perm(w[0][k], w[1][k], 0x5140);
+      const uint32_t p1 = __byte_perm(w[0][k], w[1][k], 0x7362);
+      const uint32_t q0 = __byte_perm(w[2][k], w[3][k], 0x5140);
+      const uint32_t q1 = __byte_perm(w[2][k], w[3][k], 0x7362);
+      e4m3x4_to_f16x2x2(p0, a[2 * k][0], a[2 * k][1]);
+      e4m3x4_to_f16x2x2(q0, a[2 * k][2], a[2 * k][3]);
+      e4m3x4_to_f16x2x2(p1, a[2 * k + 1][0], a[2 * k + 1][1]);
+      e4m3x4_to_f16x2x2(q1, a[2 * k + 1][2], a[2 * k + 1][3]);
     }
   } else {
     static_assert(FMT == kFmtNvfp4 && D == 128, "unsupported V layout");
     // 16 elements per token: bytes [8g, 8g+8) of the 64-byte row, block g
-    uint2 A = lds64(boxV + ta * 64 + (Gm::swz(ta, g >> 1) << 4) + ((g & 1) << 3));
-    uint2 B = lds64(boxV + tb * 64 + (Gm::swz(tb, g >> 1) << 4) + ((g & 1) << 3));
-    uint32_t sa = lds8(boxVs + ta * 8 + g), sb = lds8(boxVs + tb * 8 + g);
-    if (!va) { A = make_uint2(0, 0); sa = 0; }
-    if (!vb) { B = make_uint2(0, 0); sb = 0; }
-    uint32_t s2 = e4m3x2_to_f16x2(sa | (sb << 8));   // (scale_a, scale_b)
-    uint32_t a[2] = {A.x, A.y}, bb[2] = {B.x, B.y};
+    uint2 v[4];
+    uint32_t sc[4];
 #pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      uint32_t ev = (a[w] & 0x0F0F0F0Fu) | ((bb[w] & 0x0F0F0F0Fu) << 4);
-      uint32_t od = ((a[w] >> 4) & 0x0F0F0F0Fu) | (bb[w] & 0xF0F0F0F0u);
-      uint32_t e0, e1, e2, e3, o0, o1, o2, o3;
-      e2m1x8_to_f16x2x4(ev, e0, e1, e2, e3);
-      e2m1x8_to_f16x2x4(od, o0, o1, o2, o3);
-      bv[8 * w + 0] = hmul2(e0, s2);
-      bv[8 * w + 1] = hmul2(o0, s2);
-      bv[8 * w + 2] = hmul2(e1, s2);
-      bv[8 * w + 3] = hmul2(o1, s2);
-      bv[8 * w + 4] = hmul2(e2, s2);
-      bv[8 * w + 5] = hmul2(o2, s2);
-      bv[8 * w + 6] = hmul2(e3, s2);
-      bv[8 * w + 7] = hmul2(o3, s2);
+    for (int r = 0; r < 4; ++r) {
+      v[r] = lds64(boxV + tk[r] * 64 + (Gm::swz(tk[r], g >> 1) << 4) + ((g & 1) << 3));
+      sc[r] = lds8(boxVs + tk[r] * 8 + g);
+      if (tk[r] >= nvalid) {
+        v[r] = make_uint2(0, 0);
+        sc[r] = 0;
+      }
+    }
+    const uint32_t s01 = e4m3x2_to_f16x2(sc[0] | (sc[1] << 8));   // (scale_2t, scale_2t+1)
+    const uint32_t s89 = e4m3x2_to_f16x2(sc[2] | (sc[3] << 8));
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t A = k ? v[0].y : v[0].x, B = k ? v[1].y : v[1].x;
+      const uint32_t C = k ? v[2].y : v[2].x, E = k ? v[3].y : v[3].x;
+      const uint32_t evAB = (A & 0x0F0F0F0Fu) | ((B & 0x0F0F0F0Fu) << 4);
+      const uint32_t odAB = ((A >> 4) & 0x0F0F0F0Fu) | (B & 0xF0F0F0F0u);
+      const uint32_t evCE = (C & 0x0F0F0F0Fu) | ((E & 0x0F0F0F0Fu) << 4);
+      const uint32_t odCE = ((C >> 4) & 0x0F0F0F0Fu) | (E & 0xF0F0F0F0u);
+      uint32_t e[4], o[4], f[4], h[4];
+      e2m1x8_to_f16x2x4(evAB, e[0], e[1], e[2], e[3]);
+      e2m1x8_to_f16x2x4(odAB, o[0], o[1], o[2], o[3]);
+      e2m1x8_to_f16x2x4(evCE, f[0], f[1], f[2], f[3]);
+      e2m1x8_to_f16x2x4(odCE, h[0], h[1], h[2], h[3]);
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        const int i = 4 * k + bb;   // value dims (D/8) g + 8k + 2bb (+1)
+        a[i][0] = hmul2(e[bb], s01);
+        a[i][1] = hmul2(o[bb], s01);
+        a[i][2] = hmul2(f[bb], s89);
+        a[i][3] = hmul2(h[bb], s89);
+      }
     }
   }
+}
+
+// Column swizzle of the end-of-chunk O buffer [warp][head][d]: XOR-ing the
+// low bits of d with (head pair, high bits of the lane group) makes both the
+// fragment stores and the row-wise merge reads conflict-free.
+template <int D>
+__device__ __forceinline__ int obuf_swz(int head, int d) {
+  constexpr int kLog = D == 128 ? 4 : 3;   // log2(D / 8): dims per lane group
+  const int grp = d >> kLog;
+  return d ^ ((((head >> 1) & 3) | ((grp >> (5 - kLog)) << 2)) & ((D / 8) - 1));
 }
 
 __device__ __forceinline__ float quad_max(float v) {
@@ -200,13 +232,15 @@ __device__ __forceinline__ float quad_sum(float v) {
   return v;
 }
 
-template <int FMT, int D, bool PROBQ>
-__global__ void __launch_bounds__(kDecodeThreads, 1)
+// NH = number of 8-head groups (1: up to 8 query heads per kv head, 2: up to 16)
+template <int FMT, int D, bool PROBQ, int NH>
+__global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
     partial_kernel(const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PartialArgs a) {
   using Gm = Geom<FMT, D>;
   constexpr int KS = Gm::kKSteps;
-  constexpr int NT = Gm::kNT;
+  constexpr int MT = Gm::kMT;
+  constexpr int kSweeps = PROBQ ? 2 : 1;
 
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Smem sm;
@@ -219,7 +253,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
   // ring base, aligned for the 128-byte swizzle pattern
   const uint32_t ring = (smem_u32(dyn_smem) + 1023u) & ~1023u;
-  const uint32_t scores = ring + kStages * Gm::kStage;   // FP8-prob mode only
+  const uint32_t scores = ring + Gm::kRing;   // FP8-prob mode only
 
   // chunk of this split
   int L = a.seq_lens[b];
@@ -232,347 +266,375 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   c = (c + 15) / 16 * 16;
   const int cstart = (int)min((long)split * c, (long)L);
   const int cend = (int)min((long)cstart + c, (long)L);
-  const int ntiles = (cend - cstart + kTileTokens - 1) / kTileTokens;
-  constexpr int kSweeps = PROBQ ? 2 : 1;
+  const int nboxes = (cend - cstart + kBoxTokens - 1) / kBoxTokens;
+  // this warp's boxes: warp, warp + 4, ...
+  const int nw = nboxes > warp ? (nboxes - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
+  const int total = kSweeps * nw;
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(smem_u32(&sm.full[i]), 1);
-      mbar_init(smem_u32(&sm.empty[i]), kConsumerWarps);
+  // block-table entries of the chunk -> shared memory
+  const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
+  const int p0 = cstart / a.ps;
+  const int npages = cend > cstart ? (cend - 1) / a.ps - p0 + 1 : 0;
+  for (int i = threadIdx.x; i < min(npages, kPageCache); i += kDecodeThreads) {
+    int pg = __ldg(bt + p0 + i);
+    if (pg < 0 || pg >= a.num_pages) {
+      record_error(a.error_flag, 4);
+      pg = 0;
     }
-    sm.abort_flag = 0;
+    sm.pages[i] = pg;
+  }
+  if (threadIdx.x == 0) sm.abort_flag = 0;
+  if (lane == 0) {
+    for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&sm.full[warp][i]), 1);
     fence_barrier_init();
   }
   __syncthreads();
   volatile int* abort_flag = &sm.abort_flag;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // The whole warp walks the loop (uniform control flow); lane 0 issues.
-    if (ntiles > 0) {
-      if (lane == 0) {
-        prefetch_tmap(&tmK);
-        prefetch_tmap(&tmV);
-      }
-      const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
-      int last_pidx = -1, last_page = 0;
-      int it = 0;
-      bool ok = true;
-      for (int sweep = 0; sweep < kSweeps && ok; ++sweep) {
-        const bool loadK = !PROBQ || sweep == 0;
-        const bool loadV = !PROBQ || sweep == 1;
-        for (int tile = 0; tile < ntiles; ++tile, ++it) {
-          const int st = it % kStages;
-          if (it >= kStages) {
-            const bool got =
-                wait_or_abort(smem_u32(&sm.empty[st]), ((it / kStages) - 1) & 1, abort_flag);
-            if (!__all_sync(0xffffffffu, got)) {
-              ok = false;
-              break;
-            }
-          }
-          if (lane == 0) {
-            const int t0 = cstart + tile * kTileTokens;
-            const int nbox =
-                min(kTileTokens / kBoxTokens, (cend - t0 + kBoxTokens - 1) / kBoxTokens);
-            uint32_t bytes = 0;
-            if (loadK) bytes += nbox * (Gm::kBoxK + Gm::kBoxS);
-            if (loadV) bytes += nbox * (Gm::kBoxK + Gm::kBoxS);
-            const uint32_t full = smem_u32(&sm.full[st]);
-            mbar_arrive_expect_tx(full, bytes);
-            const uint32_t sbase = ring + st * Gm::kStage;
-            for (int bx = 0; bx < nbox; ++bx) {
-              const int tok = t0 + bx * kBoxTokens;
-              const int pidx = tok / a.ps;
-              if (pidx != last_pidx) {
-                last_pidx = pidx;
-                last_page = __ldg(bt + pidx);
-                if (last_page < 0 || last_page >= a.num_pages) {
-                  record_error(a.error_flag, 4);
-                  last_page = 0;
-                }
-              }
-              const long row = ((long)last_page * a.Hkv + h) * a.ps + (tok % a.ps);
-              if (loadK) tma_load_2d(sbase + bx * Gm::kBoxK, &tmK, 0, (int)row, full);
-              if (loadV)
-                tma_load_2d(sbase + Gm::kTileK + bx * Gm::kBoxK, &tmV, 0, (int)row, full);
-              if constexpr (FMT == kFmtNvfp4) {
-                if (loadK)
-                  bulk_load(sbase + 2 * Gm::kTileK + bx * Gm::kBoxS,
-                            a.k_bscale + row * Gm::kSRow, Gm::kBoxS, full);
-                if (loadV)
-                  bulk_load(sbase + 2 * Gm::kTileK + Gm::kTileS + bx * Gm::kBoxS,
-                            a.v_bscale + row * Gm::kSRow, Gm::kBoxS, full);
-              }
-            }
-          }
-          __syncwarp();
-        }
-      }
-      if (!ok && lane == 0) {
-        *abort_flag = 1;
-        record_error(a.error_flag, 1);
-      }
-      // Drain: no copy may still be writing shared memory when the CTA exits.
-      for (int k = max(0, it - kStages); k < it; ++k)
-        mbar_wait(smem_u32(&sm.full[k % kStages]), (k / kStages) & 1);
-      __syncwarp();
-    }
-  } else {
-    // ------------------------------------------------------------ consumers
-    const int cw = warp - 1;
-    const int hq0 = h * a.G;
-    // Q fragments, head-dim permuted like the K fragments
-    uint32_t qa[KS][4];
-    {
-      const int rows[2] = {g, g + 8};
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int row = rows[half];
-        const bool valid = row < a.G;
-        const uint16_t* qp = a.q + ((size_t)b * a.Hq + hq0 + (valid ? row : 0)) * D + (D / 4) * t;
-#pragma unroll
-        for (int j = 0; j < KS; ++j) {
-          uint2 v = valid ? *reinterpret_cast<const uint2*>(qp + 4 * j) : make_uint2(0, 0);
-          float f0 = bf16_bits_to_f32(v.x & 0xFFFFu), f1 = bf16_bits_to_f32(v.x >> 16);
-          float f2 = bf16_bits_to_f32(v.y & 0xFFFFu), f3 = bf16_bits_to_f32(v.y >> 16);
-          qa[j][half] = pack_f16x2(f0, f1);       // a0 / a1
-          qa[j][half + 2] = pack_f16x2(f2, f3);   // a2 / a3
-        }
+  // Issue the copies of this warp's j-th load (lane 0 only): load j covers
+  // box w + 4 (j % nw); in FP8-prob mode loads [0, nw) bring K, [nw, 2nw) V.
+  auto issue = [&](int j) {
+    const int sweep = PROBQ ? j / nw : 0;
+    const int box = warp + kDecodeWarps * (j - sweep * nw);
+    const bool loadK = !PROBQ || sweep == 0;
+    const bool loadV = !PROBQ || sweep == 1;
+    const int tok = cstart + box * kBoxTokens;
+    const int pidx = tok / a.ps;
+    int page;
+    if (pidx - p0 < kPageCache) {
+      page = sm.pages[pidx - p0];
+    } else {
+      page = __ldg(bt + pidx);
+      if (page < 0 || page >= a.num_pages) {
+        record_error(a.error_flag, 4);
+        page = 0;
       }
     }
+    const long row = ((long)page * a.Hkv + h) * a.ps + (tok % a.ps);
+    const int st = j % kStages;
+    const uint32_t full = smem_u32(&sm.full[warp][st]);
+    const uint32_t sbase = ring + (warp * kStages + st) * Gm::kStage;
+    const uint32_t bytes = (loadK ? Gm::kBoxK + Gm::kBoxS : 0) + (loadV ? Gm::kBoxK + Gm::kBoxS : 0);
+    mbar_arrive_expect_tx(full, bytes);
+    if (loadK) {
+      tma_load_2d(sbase, &tmK, 0, (int)row, full);
+      if constexpr (FMT == kFmtNvfp4)
+        bulk_load(sbase + 2 * Gm::kBoxK, a.k_bscale + row * Gm::kSRow, Gm::kBoxS, full);
+    }
+    if (loadV) {
+      tma_load_2d(sbase + Gm::kBoxK, &tmV, 0, (int)row, full);
+      if constexpr (FMT == kFmtNvfp4)
+        bulk_load(sbase + 2 * Gm::kBoxK + Gm::kBoxS, a.v_bscale + row * Gm::kSRow, Gm::kBoxS,
+                  full);
+    }
+  };
 
-    float o[NT][4];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    bool aborted = false;
-    int it = 0;
+  int issued = 0;
+  if (lane == 0) {
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    for (; issued < min(total, kStages); ++issued) issue(issued);
+  }
 
-    for (int sweep = 0; sweep < kSweeps; ++sweep) {
-      for (int tile = 0; tile < ntiles && !aborted; ++tile, ++it) {
-        const int st = it % kStages;
-        const bool got = wait_or_abort(smem_u32(&sm.full[st]), (it / kStages) & 1, abort_flag);
-        if (!__all_sync(0xffffffffu, got)) {
-          aborted = true;
-          break;
-        }
-        const int tbase = cstart + tile * kTileTokens + cw * kBoxTokens;
-        const int nvalid = max(0, min(kBoxTokens, cend - tbase));
-        const uint32_t sbase = ring + st * Gm::kStage;
-        const uint32_t boxK = sbase + cw * Gm::kBoxK;
-        const uint32_t boxV = sbase + Gm::kTileK + cw * Gm::kBoxK;
-        const uint32_t boxKs = sbase + 2 * Gm::kTileK + cw * Gm::kBoxS;
-        const uint32_t boxVs = sbase + 2 * Gm::kTileK + Gm::kTileS + cw * Gm::kBoxS;
-        const int tok_in_chunk = tbase - cstart;
+  const int hq0 = h * a.G;
+  // Q^T fragments (B operand of S^T = K Q^T: k = head dims, n = query heads
+  // g + 8 hh), head dims permuted like the K fragments
+  uint32_t qb[KS][NH][2];
+#pragma unroll
+  for (int hh = 0; hh < NH; ++hh) {
+    const int head = g + 8 * hh;
+    const bool valid = head < a.G;
+    const uint16_t* qp = a.q + ((size_t)b * a.Hq + hq0 + (valid ? head : 0)) * D + (D / 4) * t;
+#pragma unroll
+    for (int j = 0; j < KS; ++j) {
+      uint2 v = valid ? *reinterpret_cast<const uint2*>(qp + 4 * j) : make_uint2(0, 0);
+      qb[j][hh][0] = pack_f16x2(bf16_bits_to_f32(v.x & 0xFFFFu), bf16_bits_to_f32(v.x >> 16));
+      qb[j][hh][1] = pack_f16x2(bf16_bits_to_f32(v.y & 0xFFFFu), bf16_bits_to_f32(v.y >> 16));
+    }
+  }
 
-        if (nvalid > 0) {
-          float x[2][4];
-          if (!PROBQ || sweep == 0) {
-            // ---- scores S = Q K^T for the box's 16 tokens (two n-tiles)
+  // O^T accumulators: m-tile i (value dims), head group hh; C layout
+  // c0,c1 = (dim row g, heads 2t, 2t+1), c2,c3 = (dim row g+8, same heads)
+  float o[MT][NH][4];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              uint32_t kb[KS][2];
-              k_frag<FMT, D>(boxK, boxKs, 8 * u + g, t, kb);
-              float s[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int i = 0; i < MT; ++i)
 #pragma unroll
-              for (int j = 0; j < KS; ++j)
-                mma_f16(s, qa[j][0], qa[j][1], qa[j][2], qa[j][3], kb[j][0], kb[j][1]);
+    for (int hh = 0; hh < NH; ++hh) o[i][hh][0] = o[i][hh][1] = o[i][hh][2] = o[i][hh][3] = 0.f;
+  // reference max (log2 domain) and partial denominator of heads
+  // 2t + e + 8 hh -- the same heads as this lane's S^T and O^T columns
+  float m[NH][2], l[NH][2];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int tk = 8 * u + 2 * t + (e & 1);
-                x[u][e] = tk < nvalid ? s[e] * a.qk_scale_log2 : -INFINITY;
-              }
-            }
+  for (int hh = 0; hh < NH; ++hh) m[hh][0] = m[hh][1] = -INFINITY, l[hh][0] = l[hh][1] = 0.f;
+  bool aborted = false;
+
+  for (int sweep = 0; sweep < kSweeps; ++sweep) {
+    for (int jj = 0; jj < nw && !aborted; ++jj) {
+      const int j = sweep * nw + jj;
+      const int st = j % kStages;
+      // one lane polls the barrier; the vote tells the warp the outcome
+      bool got = true;
+      if (lane == 0)
+        got = wait_or_abort(smem_u32(&sm.full[warp][st]), (j / kStages) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        aborted = true;
+        break;
+      }
+      __syncwarp();   // the other lanes read the box after lane 0's acquire
+      const int tbase = cstart + (warp + kDecodeWarps * jj) * kBoxTokens;
+      const int nvalid = min(kBoxTokens, cend - tbase);
+      const uint32_t sbase = ring + (warp * kStages + st) * Gm::kStage;
+      const uint32_t boxK = sbase;
+      const uint32_t boxV = sbase + Gm::kBoxK;
+      const uint32_t boxKs = sbase + 2 * Gm::kBoxK;
+      const uint32_t boxVs = boxKs + Gm::kBoxS;
+      const int tok_in_chunk = tbase - cstart;
+
+      // x[hh][e]: scaled score of token g + 8 (e >> 1), head 2t + (e & 1) + 8 hh
+      float x[NH][4];
+      if (!PROBQ || sweep == 0) {
+        uint32_t kg[KS][2], kg8[KS][2];
+        k_frag<FMT, D>(boxK, boxKs, g, t, kg);
+        k_frag<FMT, D>(boxK, boxKs, g + 8, t, kg8);
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) {
+          // two accumulators halve the dependent MMA chain
+          float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kk = 0; kk < KS; kk += 2) {
+            mma_f16(s0, kg[kk][0], kg8[kk][0], kg[kk][1], kg8[kk][1], qb[kk][hh][0],
+                    qb[kk][hh][1]);
+            mma_f16(s1, kg[kk + 1][0], kg8[kk + 1][0], kg[kk + 1][1], kg8[kk + 1][1],
+                    qb[kk + 1][hh][0], qb[kk + 1][hh][1]);
           }
-          if constexpr (PROBQ) {
-            if (sweep == 0) {
-              // keep the scores of the valid head rows; track the chunk max
 #pragma unroll
-              for (int u = 0; u < 2; ++u)
+          for (int e = 0; e < 4; ++e) x[hh][e] = (s0[e] + s1[e]) * a.qk_scale_log2;
+          if (nvalid < kBoxTokens) {   // ragged tail of the chunk
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int row = g + 8 * (e >> 1);
-                  const int tk = 8 * u + 2 * t + (e & 1);
-                  if (row < a.G && tk < nvalid) {
-                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(
-                                     scores + 4u * ((tok_in_chunk + tk) * a.G + row)),
-                                 "f"(x[u][e]));
-                  }
-                }
-              m0 = fmaxf(m0, quad_max(fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]))));
-              m1 = fmaxf(m1, quad_max(fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]))));
-            } else {
-              // ---- FP8 probabilities against the chunk max (m0/m1 hold it)
-              const float b0 = m0 == -INFINITY ? 0.f : m0;
-              const float b1 = m1 == -INFINITY ? 0.f : m1;
-              uint32_t pa[4];
-#pragma unroll
-              for (int u = 0; u < 2; ++u) {
-                float p[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int row = g + 8 * (e >> 1);
-                  const int tk = 8 * u + 2 * t + (e & 1);
-                  float xs = -INFINITY;
-                  if (row < a.G && tk < nvalid) {
-                    asm volatile("ld.shared.f32 %0, [%1];"
-                                 : "=f"(xs)
-                                 : "r"(scores + 4u * ((tok_in_chunk + tk) * a.G + row)));
-                  }
-                  p[e] = exp2f(xs - ((e >> 1) ? b1 : b0));
-                }
-                l0 += p[0] + p[1];
-                l1 += p[2] + p[3];
-                const float ps = a.prob_scale;
-                uint32_t c01 = f32x2_to_e4m3x2(__fdiv_rn(p[0], ps), __fdiv_rn(p[1], ps));
-                uint32_t c23 = f32x2_to_e4m3x2(__fdiv_rn(p[2], ps), __fdiv_rn(p[3], ps));
-                pa[2 * u + 0] = e4m3x2_to_f16x2(c01);   // row g   (a0 / a2)
-                pa[2 * u + 1] = e4m3x2_to_f16x2(c23);   // row g+8 (a1 / a3)
-              }
-              uint32_t bv0[NT], bv1[NT];
-              v_pair<FMT, D>(boxV, boxVs, 2 * t, 2 * t + 1, 2 * t < nvalid, 2 * t + 1 < nvalid, g,
-                             bv0);
-              v_pair<FMT, D>(boxV, boxVs, 2 * t + 8, 2 * t + 9, 2 * t + 8 < nvalid,
-                             2 * t + 9 < nvalid, g, bv1);
-#pragma unroll
-              for (int j = 0; j < NT; ++j) mma_f16(o[j], pa[0], pa[1], pa[2], pa[3], bv0[j], bv1[j]);
-            }
-          } else {
-            // ---- online softmax update (log2 domain)
-            const float mx0 = quad_max(fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1])));
-            const float mx1 = quad_max(fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3])));
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float b0 = mn0 == -INFINITY ? 0.f : mn0;
-            const float b1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float al0 = exp2f(m0 - b0), al1 = exp2f(m1 - b1);
-            m0 = mn0;
-            m1 = mn1;
-            float p[2][4];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              p[u][0] = exp2f(x[u][0] - b0);
-              p[u][1] = exp2f(x[u][1] - b0);
-              p[u][2] = exp2f(x[u][2] - b1);
-              p[u][3] = exp2f(x[u][3] - b1);
-            }
-            l0 = l0 * al0 + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
-            l1 = l1 * al1 + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
-            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-              for (int j = 0; j < NT; ++j) {
-                o[j][0] *= al0;
-                o[j][1] *= al0;
-                o[j][2] *= al1;
-                o[j][3] *= al1;
-              }
-            }
-            // P as f16 high part + f16 residual
-            uint32_t ph[4], pl[4];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              ph[2 * u + 0] = pack_f16x2(p[u][0], p[u][1]);
-              ph[2 * u + 1] = pack_f16x2(p[u][2], p[u][3]);
-              const float2 r0 = unpack_f16x2(ph[2 * u + 0]);
-              const float2 r1 = unpack_f16x2(ph[2 * u + 1]);
-              pl[2 * u + 0] = pack_f16x2(p[u][0] - r0.x, p[u][1] - r0.y);
-              pl[2 * u + 1] = pack_f16x2(p[u][2] - r1.x, p[u][3] - r1.y);
-            }
-            uint32_t bv0[NT], bv1[NT];
-            v_pair<FMT, D>(boxV, boxVs, 2 * t, 2 * t + 1, 2 * t < nvalid, 2 * t + 1 < nvalid, g,
-                           bv0);
-            v_pair<FMT, D>(boxV, boxVs, 2 * t + 8, 2 * t + 9, 2 * t + 8 < nvalid,
-                           2 * t + 9 < nvalid, g, bv1);
-#pragma unroll
-            for (int j = 0; j < NT; ++j) {
-              mma_f16(o[j], ph[0], ph[1], ph[2], ph[3], bv0[j], bv1[j]);
-              mma_f16(o[j], pl[0], pl[1], pl[2], pl[3], bv0[j], bv1[j]);
-            }
+            for (int e = 0; e < 4; ++e)
+              if (g + 8 * (e >> 1) >= nvalid) x[hh][e] = -INFINITY;
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
       }
       if constexpr (PROBQ) {
         if (sweep == 0) {
-          // chunk max across the consumer warps (every consumer warp takes
-          // part in both barriers, aborted or not)
-          __syncwarp();
-          if (t == 0) {
-            sm.m[cw][g] = m0;
-            sm.m[cw][g + 8] = m1;
-          }
-          asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
-          float a0 = -INFINITY, a1 = -INFINITY;
+          // keep the scores of the valid heads; track the chunk max
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            a0 = fmaxf(a0, sm.m[w][g]);
-            a1 = fmaxf(a1, sm.m[w][g + 8]);
+          for (int hh = 0; hh < NH; ++hh) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int head = 2 * t + (e & 1) + 8 * hh;
+              const int tk = g + 8 * (e >> 1);
+              if (head < a.G && tk < nvalid)
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(
+                                 scores + 4u * ((tok_in_chunk + tk) * a.G + head)),
+                             "f"(x[hh][e]));
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float mx = fmaxf(x[hh][e], x[hh][e + 2]);
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+              m[hh][e] = fmaxf(m[hh][e], mx);
+            }
           }
-          m0 = a0;
-          m1 = a1;
-          asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
+        } else {
+          // FP8 probabilities against the chunk max (m holds it)
+          uint32_t pb[NH][2];
+#pragma unroll
+          for (int hh = 0; hh < NH; ++hh) {
+            float p[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int head = 2 * t + (e & 1) + 8 * hh;
+              const int tk = g + 8 * (e >> 1);
+              float xs = -INFINITY;
+              if (head < a.G && tk < nvalid)
+                asm volatile("ld.shared.f32 %0, [%1];"
+                             : "=f"(xs)
+                             : "r"(scores + 4u * ((tok_in_chunk + tk) * a.G + head)));
+              const float mm = m[hh][e & 1];
+              p[e] = ex2(xs - (mm == -INFINITY ? 0.f : mm));
+            }
+            l[hh][0] += p[0] + p[2];
+            l[hh][1] += p[1] + p[3];
+            const float ps = a.prob_scale;
+            const uint32_t c01 =
+                e4m3x2_to_f16x2(f32x2_to_e4m3x2(__fdiv_rn(p[0], ps), __fdiv_rn(p[1], ps)));
+            const uint32_t c23 =
+                e4m3x2_to_f16x2(f32x2_to_e4m3x2(__fdiv_rn(p[2], ps), __fdiv_rn(p[3], ps)));
+            pb[hh][0] = movmatrix_trans(c01);   // (tokens 2t, 2t+1; head g)
+            pb[hh][1] = movmatrix_trans(c23);   // (tokens 2t+8, 2t+9; head g)
+          }
+          uint32_t va[MT][4];
+          v_frag<FMT, D>(boxV, boxVs, t, g, nvalid, va);
+#pragma unroll
+          for (int i = 0; i < MT; ++i)
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh)
+              mma_f16(o[i][hh], va[i][0], va[i][1], va[i][2], va[i][3], pb[hh][0], pb[hh][1]);
         }
+      } else {
+        // ---- softmax update with a lazily moving reference max
+        bool need = false;
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) need |= x[hh][e] > m[hh][e & 1] + kLazyMax;
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int hh = 0; hh < NH; ++hh)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float mx = fmaxf(x[hh][e], x[hh][e + 2]);
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+              const bool mv = mx > m[hh][e] + kLazyMax;   // also the first finite box
+              const float alpha = mv ? ex2(m[hh][e] - mx) : 1.f;
+              m[hh][e] = mv ? mx : m[hh][e];
+              l[hh][e] *= alpha;
+#pragma unroll
+              for (int i = 0; i < MT; ++i) {
+                o[i][hh][e] *= alpha;
+                o[i][hh][e + 2] *= alpha;
+              }
+            }
+        }
+        uint32_t ph[NH][2], pl[NH][2];
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) {
+          const float b0 = m[hh][0] == -INFINITY ? 0.f : m[hh][0];
+          const float b1 = m[hh][1] == -INFINITY ? 0.f : m[hh][1];
+          const float p0 = ex2(x[hh][0] - b0), p1 = ex2(x[hh][1] - b1);
+          const float p2 = ex2(x[hh][2] - b0), p3 = ex2(x[hh][3] - b1);
+          l[hh][0] += p0 + p2;
+          l[hh][1] += p1 + p3;
+          // P as f16 high part + f16 residual, moved into the P^T layout
+          const uint32_t h01 = pack_f16x2(p0, p1), h23 = pack_f16x2(p2, p3);
+          const float2 r01 = unpack_f16x2(h01), r23 = unpack_f16x2(h23);
+          ph[hh][0] = movmatrix_trans(h01);
+          ph[hh][1] = movmatrix_trans(h23);
+          pl[hh][0] = movmatrix_trans(pack_f16x2(p0 - r01.x, p1 - r01.y));
+          pl[hh][1] = movmatrix_trans(pack_f16x2(p2 - r23.x, p3 - r23.y));
+        }
+        uint32_t va[MT][4];
+        v_frag<FMT, D>(boxV, boxVs, t, g, nvalid, va);
+#pragma unroll
+        for (int i = 0; i < MT; ++i)
+#pragma unroll
+          for (int hh = 0; hh < NH; ++hh) {
+            mma_f16(o[i][hh], va[i][0], va[i][1], va[i][2], va[i][3], ph[hh][0], ph[hh][1]);
+            mma_f16(o[i][hh], va[i][0], va[i][1], va[i][2], va[i][3], pl[hh][0], pl[hh][1]);
+          }
+      }
+      // the box is consumed: refill its stage with this warp's load j + kStages
+      __syncwarp();
+      if (lane == 0 && issued < total) {
+        fence_proxy_async_shared();   // generic reads of the stage before the async overwrite
+        issue(issued++);
       }
     }
-    if (aborted) {
-      *abort_flag = 1;
-      record_error(a.error_flag, 1);
-    }
-    // per-warp state -> shared memory
-    l0 = quad_sum(l0);
-    l1 = quad_sum(l1);
-    if (t == 0) {
-      sm.m[cw][g] = m0;
-      sm.m[cw][g + 8] = m1;
-      sm.l[cw][g] = l0;
-      sm.l[cw][g + 8] = l1;
-    }
-    // O tiles go to the (drained) ring: obuf[cw][row][d], rows < G
-    __syncwarp();
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
-    float* obuf = reinterpret_cast<float*>(dyn_smem + (ring - smem_u32(dyn_smem)));
-    if (!*abort_flag) {
+    if constexpr (PROBQ) {
+      if (sweep == 0) {
+        // chunk max across the warps (every warp takes part, aborted or not)
+        __syncwarp();
+        if (g == 0) {
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
+          for (int hh = 0; hh < NH; ++hh) {
+            sm.m[warp][2 * t + 8 * hh] = m[hh][0];
+            sm.m[warp][2 * t + 1 + 8 * hh] = m[hh][1];
+          }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float mm = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kDecodeWarps; ++w) mm = fmaxf(mm, sm.m[w][2 * t + e + 8 * hh]);
+            m[hh][e] = mm;
+          }
+        __syncthreads();
+      }
+    }
+  }
+  if (aborted) {
+    *abort_flag = 1;
+    record_error(a.error_flag, 1);
+  }
+  // Drain: no copy of this warp may still be writing shared memory later.
+  if (lane == 0) {
+    const int done = aborted ? 0 : total;
+    for (int k = max(done, issued - kStages); k < issued; ++k)
+      mbar_wait(smem_u32(&sm.full[warp][k % kStages]), (k / kStages) & 1);
+  }
+  __syncwarp();
+  // per-warp state -> shared memory (m is uniform over the 8 lanes of a
+  // head; l is summed over them)
+#pragma unroll
+  for (int hh = 0; hh < NH; ++hh)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float v = l[hh][e];
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      l[hh][e] = v;
+    }
+  if (g == 0) {
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        sm.m[warp][2 * t + e + 8 * hh] = m[hh][e];
+        sm.l[warp][2 * t + e + 8 * hh] = l[hh][e];
+      }
+  }
+  // O tiles go to the (drained) ring: obuf[warp][head][swizzled d], heads < G
+  __syncthreads();
+  float* obuf = reinterpret_cast<float*>(dyn_smem + (ring - smem_u32(dyn_smem)));
+  const bool bad = *abort_flag != 0;
+  if (!bad) {
+#pragma unroll
+    for (int i = 0; i < MT; ++i)
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int row = g + 8 * (e >> 1);
-          const int col = 2 * t + (e & 1);
-          const int d = (D / 8) * col + j;
-          if (row < a.G) obuf[(cw * a.G + row) * D + d] = o[j][e];
+          const int head = 2 * t + (e & 1) + 8 * hh;
+          const int d = (D / 8) * g + 2 * i + (e >> 1);
+          if (head < a.G) obuf[(warp * a.G + head) * D + obuf_swz<D>(head, d)] = o[i][hh][e];
         }
-      }
-    }
   }
   __syncthreads();
 
   // ---------------------------------------------------------------- merge
   const size_t part_row = ((size_t)b * a.Hq + (size_t)h * a.G);   // first query head
-  const bool bad = *abort_flag != 0;
   if (threadIdx.x < a.G) {
     const int row = threadIdx.x;
     float M = -INFINITY;
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.m[w][row]);
+    for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, sm.m[w][row]);
     float Ltot = 0.f;
-    for (int w = 0; w < kConsumerWarps; ++w)
-      if (sm.m[w][row] != -INFINITY) Ltot += exp2f(sm.m[w][row] - M) * sm.l[w][row];
-    for (int w = 0; w < kConsumerWarps; ++w)
-      sm.fac[w][row] = (M == -INFINITY || sm.m[w][row] == -INFINITY)
+    for (int w = 0; w < kDecodeWarps; ++w)
+      if (sm.m[w][row] != -INFINITY) Ltot += ex2(sm.m[w][row] - M) * sm.l[w][row];
+    for (int w = 0; w < kDecodeWarps; ++w)
+      sm.fac[w][row] = (M == -INFINITY || sm.m[w][row] == -INFINITY || Ltot == 0.f)
                            ? 0.f
-                           : exp2f(sm.m[w][row] - M) / Ltot * a.out_mult;
-    float lse = (M == -INFINITY) ? -INFINITY : (M + log2f(Ltot)) * kLn2;
+                           : ex2(sm.m[w][row] - M) / Ltot * a.out_mult;
+    float lse = (M == -INFINITY || Ltot == 0.f) ? -INFINITY : (M + log2f(Ltot)) * kLn2;
     if (bad) lse = NAN;
     a.part_lse[(part_row + row) * a.num_splits + split] = lse;
   }
   __syncthreads();
-  const float* obuf = reinterpret_cast<const float*>(dyn_smem + (ring - smem_u32(dyn_smem)));
   for (int i = threadIdx.x; i < a.G * D; i += blockDim.x) {
     const int row = i / D, d = i % D;
     float acc = 0.f;
     if (!bad) {
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) acc += sm.fac[w][row] * obuf[(w * a.G + row) * D + d];
+      for (int w = 0; w < kDecodeWarps; ++w)
+        acc += sm.fac[w][row] * obuf[(w * a.G + row) * D + obuf_swz<D>(row, d)];
     } else {
       acc = NAN;
     }
@@ -621,36 +683,40 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
   }
 }
 
-template <int FMT, int D, bool PROBQ>
-cudaError_t launch_partial_t(const CUtensorMap& tk, const CUtensorMap& tv, const PartialArgs& a,
-                             cudaStream_t st) {
+template <int FMT, int D, bool PROBQ, int NH>
+cudaError_t launch_partial_t(const TensorMaps& m, const PartialArgs& a, cudaStream_t st) {
   using Gm = Geom<FMT, D>;
-  size_t smem = 1024 + (size_t)kStages * Gm::kStage;
-  if (PROBQ) smem += (size_t)kScoreCapacity * 4;
-  // the merge buffer reuses the ring
-  const size_t merge = (size_t)kConsumerWarps * kMaxGroup * D * 4;
-  if (1024 + (size_t)kStages * Gm::kStage < 1024 + merge) smem = 1024 + merge + (PROBQ ? (size_t)kScoreCapacity * 4 : 0);
-  auto kern = partial_kernel<FMT, D, PROBQ>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static_assert((size_t)kDecodeWarps * kMaxGroup * D * 4 <= (size_t)Gm::kRing,
+                "the merge buffer must fit in the ring");
+  const size_t smem = 1024 + (size_t)Gm::kRing + (PROBQ ? (size_t)kScoreCapacity * 4 : 0);
+  auto kern = partial_kernel<FMT, D, PROBQ, NH>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   dim3 grid(a.batch * a.Hkv, a.num_splits);
-  kern<<<grid, kDecodeThreads, smem, st>>>(tk, tv, a);
+  kern<<<grid, kDecodeThreads, smem, st>>>(m.k16, m.v16, a);
   return cudaGetLastError();
+}
+
+template <int FMT, int D>
+cudaError_t dispatch_nh(bool probq, const TensorMaps& m, const PartialArgs& a, cudaStream_t st) {
+  if (a.G <= 8)
+    return probq ? launch_partial_t<FMT, D, true, 1>(m, a, st)
+                 : launch_partial_t<FMT, D, false, 1>(m, a, st);
+  return probq ? launch_partial_t<FMT, D, true, 2>(m, a, st)
+               : launch_partial_t<FMT, D, false, 2>(m, a, st);
 }
 
 }  // namespace
 
-cudaError_t launch_partial(int fmt, int D, bool probq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const PartialArgs& a, cudaStream_t st) {
-  if (fmt == kFmtFp8 && D == 128)
-    return probq ? launch_partial_t<kFmtFp8, 128, true>(tk, tv, a, st)
-                 : launch_partial_t<kFmtFp8, 128, false>(tk, tv, a, st);
-  if (fmt == kFmtFp8 && D == 64)
-    return probq ? launch_partial_t<kFmtFp8, 64, true>(tk, tv, a, st)
-                 : launch_partial_t<kFmtFp8, 64, false>(tk, tv, a, st);
-  if (fmt == kFmtNvfp4 && D == 128)
-    return probq ? launch_partial_t<kFmtNvfp4, 128, true>(tk, tv, a, st)
-                 : launch_partial_t<kFmtNvfp4, 128, false>(tk, tv, a, st);
+cudaError_t launch_partial(int fmt, int D, bool probq, const TensorMaps& m, const PartialArgs& a,
+                           cudaStream_t st) {
+  if (fmt == kFmtFp8 && D == 128) return dispatch_nh<kFmtFp8, 128>(probq, m, a, st);
+  if (fmt == kFmtFp8 && D == 64) return dispatch_nh<kFmtFp8, 64>(probq, m, a, st);
+  if (fmt == kFmtNvfp4 && D == 128) return dispatch_nh<kFmtNvfp4, 128>(probq, m, a, st);
   return cudaErrorInvalidValue;
 }
 

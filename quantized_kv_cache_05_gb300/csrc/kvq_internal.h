@@ -13,13 +13,13 @@ constexpr int kFmtFp8 = 1;
 constexpr int kFmtNvfp4 = 2;
 
 // Decode pipeline geometry shared by host and device code.
-constexpr int kTileTokens = 64;   // tokens per pipeline stage
-constexpr int kBoxTokens = 16;    // rows per TMA box (one 16-token page)
-constexpr int kConsumerWarps = 4; // each consumes one 16-token box per stage
-constexpr int kDecodeThreads = 32 * (1 + kConsumerWarps);
-constexpr int kStages = 4;
-constexpr int kMaxGroup = 16;     // query heads per kv head (MMA M = 16)
+constexpr int kBoxTokens = 16;    // tokens per TMA box (one 16-token page) = one MMA k-tile
+constexpr int kDecodeWarps = 4;   // each warp streams and consumes its own boxes
+constexpr int kDecodeThreads = 32 * kDecodeWarps;
+constexpr int kStages = 4;        // boxes in flight per warp
+constexpr int kMaxGroup = 16;     // query heads per kv head (two 8-head MMA tiles)
 constexpr int kScoreCapacity = 16384;  // fp32 scores per CTA in FP8-prob mode
+constexpr int kPageCache = 1024;  // block-table entries of a chunk kept in shared memory
 
 struct AppendArgs {
   int fmt, D, Hkv, ps, max_pages, batch, T, rope, num_pages;
@@ -64,8 +64,13 @@ struct CombineArgs {
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_amax_bf16(const uint16_t* x, size_t n, float* out, cudaStream_t st);
 cudaError_t launch_encode(int kind, const float* x, uint8_t* out, size_t n, cudaStream_t st);
-cudaError_t launch_partial(int fmt, int D, bool probq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const PartialArgs& a, cudaStream_t st);
+// TMA descriptors of the K and V code tensors (16-row boxes).
+struct TensorMaps {
+  CUtensorMap k16, v16;
+};
+
+cudaError_t launch_partial(int fmt, int D, bool probq, const TensorMaps& m, const PartialArgs& a,
+                           cudaStream_t st);
 cudaError_t launch_mla_partial(const CUtensorMap& tk, const PartialArgs& a, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 

@@ -60,16 +60,19 @@ def test_tensor_scale_matches_oracle(orc):
 
 def test_auto_splits():
     f = kvq.kvq_auto_splits
-    # 152 SMs, GQA 2 x 8 kv heads: ceil(304/16) = 19, long sequences keep it
-    assert f(152, 2, 8, 4, 32768, 1) == (0, 19)
-    assert f(152, 2, 8, 4, 8192, 1) == (0, 19)
-    # short sequences: at least 256 tokens per chunk
-    assert f(152, 2, 8, 4, 1024, 1) == (0, 4)
+    # 152 SMs, GQA 2 x 8 kv heads: floor(3 * 152 / 16) = 28 (one wave of 448 CTAs)
+    assert f(152, 2, 8, 4, 32768, 1) == (0, 28)
+    assert f(152, 2, 8, 4, 8192, 1) == (0, 28)
+    # short sequences: at least 128 tokens per chunk
+    assert f(152, 2, 8, 4, 1024, 1) == (0, 8)
     assert f(152, 2, 8, 4, 100, 1) == (0, 1)
-    # batch 1 x 8 kv heads: ceil(304/8) = 38
-    assert f(152, 1, 8, 4, 32768, 2) == (0, 38)
+    # batch 1 x 8 kv heads: floor(456 / 8) = 57
+    assert f(152, 1, 8, 4, 32768, 2) == (0, 57)
+    assert f(152, 1, 8, 4, 2048, 2) == (0, 16)
     # large batch: one split
     assert f(152, 64, 16, 1, 8192, 1) == (0, 1)
+    # MLA: base = batch = 32 -> floor(456 / 32) = 14
+    assert f(152, 32, 1, 16, 4096, 2) == (0, 14)
     # clamp at 64
     assert f(152, 1, 1, 16, 1 << 20, 2) == (0, 64)
     assert f(0, 1, 1, 1, 10, 1)[0] == kvq.KVQ_ERR_INVALID

@@ -123,6 +123,30 @@ def test_paged_exact_probabilities_off():
     assert_f32_close(out.cpu().numpy(), ref, "paged exact")
 
 
+@pytest.mark.parametrize("hq,hkv,fmt", [(16, 1, "fp8"), (24, 2, "fp8"), (16, 2, "nvfp4"),
+                                         (12, 1, "nvfp4")])
+def test_large_groups(hq, hkv, fmt):
+    """9..16 query heads per kv head (two head groups of the P.V MMA)."""
+    w = synth.gqa_fp8(700) if fmt == "fp8" else synth.nvfp4(700)
+    w.B, w.Hq, w.Hkv = 2, hq, hkv
+    w.seq_lens = np.array([700, 333], np.int32)
+    S = Setup(w)
+    ref, _ = S.oracle_decode()
+    for s in (1, 3):
+        out, _ = S.gpu_decode(s)
+        assert_f32_close(out.cpu().numpy(), ref, f"G={hq // hkv} {fmt} s={s}")
+
+
+def test_large_groups_fp8_probs():
+    w = synth.paged_fp8_probs(B=3, lo=40, hi=500, seed=11)
+    w.Hq, w.Hkv = 16, 1
+    S = Setup(w)
+    for s in (1, 2):
+        ref, _ = S.oracle_decode(mode=1, s=s)
+        out, _ = S.gpu_decode(s)
+        assert_f32_close(out.cpu().numpy(), ref, f"G=16 probs s={s}")
+
+
 def test_edge_lengths():
     """Lengths 0 (output 0), 1, 15, 16, 17 and fewer tokens than splits."""
     w = synth.gqa_fp8(64)
