@@ -1,9 +1,9 @@
 """Benchmark: split-KV decode over a quantized KV cache on one GB300.
 
 One step = the whole decode hot path for one new token per request:
-quantize-on-append of the new K/V rows, the split-KV partial kernel and the
-combine kernel (split count from kvq_auto_splits), over a cache of kv_len
-tokens per request that is resident in HBM.  The headline workload is GQA
+quantize-on-append of the new K/V rows, then the split-KV decode with its
+combine in one launch (kvq_decode; split count from kvq_auto_splits), over a
+cache of kv_len tokens per request that is resident in HBM.  The headline workload is GQA
 4:1 FP8: batch 2, 32 query / 8 kv heads, head_dim 128, kv_len 32768, 1% of
 elements x10, bf16 output.
 
@@ -11,7 +11,7 @@ Timing: W warm-up steps, then K timed steps; before every timed step the L2
 is flushed by writing one 256 MiB buffer and then reading another (the read
 evicts the written lines, so the timed step neither finds its data in L2 nor
 pays for write-backs of the flush), and each step is bracketed by CUDA events
-on the launch stream (the three launches are replayed as one CUDA graph).
+on the launch stream (the two launches are replayed as one CUDA graph).
 `value` is the mean device time per step in microseconds (lower is better); KV GB/s = attended cache bytes / step time.
 
     python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
@@ -211,7 +211,7 @@ class Bench:
             kvq.check(kvq.kvq_amax_bf16(ob, ob.numel(), a, self.stream))
             self.out_scale = kvq.kvq_tensor_scale(kvq.KVQ_FP8_E4M3, float(a.item()) * 1.01)[1]
         self.cfg = self._cfg(w.out, self.out_scale)
-        self.ws = runtime.DecodeWorkspace(self.cfg, device)
+        self.ws = runtime.FusedWorkspace(self.cfg, w.Hkv, device)
         self.flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
         self.flush_rd = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
         self.flush_sink = torch.zeros(1, dtype=torch.float32, device=device)
@@ -229,16 +229,15 @@ class Bench:
                                          w.Lmax, w.sm_scale, w.prob_scale, out, out_scale)
 
     def _launch(self, full: bool, stream):
+        """full: append + kvq_decode (one step); else kvq_decode alone."""
         kvq = self.kvq
         c = self.cache.struct()
         p = self.cfg.params(self.seq_lens)
         if full:
             kvq.check(kvq.kvq_quantize_append(c, self.k_new, self.v_new, self.kpe_new,
                                               self.start_pos, self.w.B, 1, stream))
-        kvq.check(kvq.kvq_decode_partial(c, p, self.q, self.ws.part_o, self.ws.part_lse, stream))
-        if full:
-            kvq.check(kvq.kvq_decode_combine(p, self.ws.part_o, self.ws.part_lse, self.ws.out,
-                                             stream))
+        kvq.check(kvq.kvq_decode(c, p, self.q, self.ws.part_o, self.ws.part_lse, self.ws.counters,
+                                 self.ws.out, stream))
 
     def _capture(self, full: bool):
         t = self.torch
@@ -315,14 +314,16 @@ class Bench:
         return tok * per
 
     def partial_bytes(self) -> int:
-        """Algorithmic bytes of one partial launch: attended cache bytes,
-        block-table entries, Q, and the partial outputs written."""
+        """Algorithmic bytes of one kvq_decode launch: attended cache bytes,
+        block-table entries and Q read; split partials written and read back
+        by the merging CTA; the output written."""
         w = self.w
         ps = w.page_size_eff()
         bt = int(sum(-(-int(L) // ps) for L in w.seq_lens)) * 4 * (1 if w.mla else w.Hkv)
         q = w.B * w.Hq * w.Dqk * 2
-        parts = w.B * w.Hq * self.splits * (w.Dv + 1) * 4
-        return self.kv_bytes() + bt + q + parts
+        parts = 2 * w.B * w.Hq * self.splits * (w.Dv + 1) * 4
+        out = w.B * w.Hq * w.Dv * self.ws.out.element_size()
+        return self.kv_bytes() + bt + q + parts + out
 
 
 def run_ours(args):
@@ -376,7 +377,7 @@ def run_ours(args):
             "workload": f"gqa_fp8: batch 2, Hq 32, Hkv 8, head_dim 128, kv_len {args.kv_len}, "
                         f"FP8 E4M3 per-tensor KV, bf16 out, s=auto",
             "batch": w.B, "kv_len": args.kv_len, "splits": bench.splits,
-            "step": "append 1 token + split-KV partial + combine (one CUDA graph)",
+            "step": "append 1 token + kvq_decode (partial with fused combine), one CUDA graph",
             "l2": "flushed before every timed step (256 MiB write, then 256 MiB read)",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
@@ -385,7 +386,7 @@ def run_ours(args):
         "kv_hbm_frac": round(kvb / (us * 1e-6) / 1e9 / peak, 4),
         "partial_us": round(part, 3),
         "roofline": {
-            "kernel": "partial_kernel<FP8,128>",
+            "kernel": "partial_kernel<FP8,128> (kvq_decode, fused combine)",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -397,7 +398,7 @@ def run_ours(args):
         },
         "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},
-        "gpu_launches": 3 * args.steps + args.steps,
+        "gpu_launches": 2 * args.steps + args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_sweep:
@@ -447,7 +448,7 @@ def _with_splits(self, s):
     nb.splits = s or self.runtime.auto_splits(self.w.B, self.w.Hkv, self.w.G, self.w.Lmax,
                                               self.w.fmt, self.device)
     nb.cfg = nb._cfg(self.w.out, self.out_scale)
-    nb.ws = self.runtime.DecodeWorkspace(nb.cfg, self.device)
+    nb.ws = self.runtime.FusedWorkspace(nb.cfg, self.w.Hkv, self.device)
     nb.graph_step = nb._capture(full=True)
     nb.graph_partial = None
     return nb

@@ -112,7 +112,7 @@ typedef struct kvq_decode_params {
   int32_t num_q_heads;       /* Hq, a multiple of Hkv; Hq/Hkv <= 16 */
   int32_t qk_dim;            /* head_dim (MLA: 512 + 64 = 576) */
   int32_t v_dim;             /* head_dim (MLA: 512) */
-  int32_t num_splits;        /* s >= 1 (see kvq_auto_splits) */
+  int32_t num_splits;        /* 1 <= s <= 64 (see kvq_auto_splits) */
   const int32_t* seq_lens;   /* (device) [batch] tokens per request */
   int32_t max_kv_len;        /* (host) upper bound of seq_lens[] */
   float sm_scale;            /* softmax scale (e.g. 1/sqrt(head_dim)) */
@@ -192,7 +192,8 @@ size_t kvq_partial_workspace_bytes(int batch, int num_q_heads, int num_splits, i
  *   p_q = dec(E4M3(fl32(p~ / prob_scale))) * prob_scale, p~ = exp(S_i - m)
  * in fp32 with m the chunk max, while l sums the unquantized p~.
  *   q (device) bf16 [batch][Hq][qk_dim], 16-byte aligned.
- *   part_o, part_lse (device) as in kvq_partial_workspace_bytes.
+ *   part_o, part_lse (device) as in kvq_partial_workspace_bytes; part_o
+ *   16-byte aligned.
  * With prob_scale > 0 one chunk's scores must fit in on-chip memory:
  * ceil(max_kv_len / s) rounded up to 16, times Hq/Hkv, at most 16384;
  * larger chunks return KVQ_ERR_UNSUPPORTED (raise num_splits).
@@ -209,6 +210,22 @@ kvq_status kvq_decode_partial(const kvq_cache* c, const kvq_decode_params* p, co
  */
 kvq_status kvq_decode_combine(const kvq_decode_params* p, const float* part_o,
                               const float* part_lse, void* out, void* stream);
+
+/*
+ * One decode step in a single launch: kvq_decode_partial followed by the
+ * merge of kvq_decode_combine, which the last CTA to finish for each
+ * (request, kv head) performs with the same arithmetic and output types.
+ *   part_o, part_lse (device) split partials, as for kvq_decode_partial.
+ *   counters (device) uint32 [batch * num_kv_heads] arrival counters.  They
+ *   must be zero before the first call; every call leaves them at zero
+ *   again, so one zero-filled array (sized for the largest batch *
+ *   num_kv_heads) serves any number of later calls.  Calls that share
+ *   counters or partials must not overlap on the GPU (stream-order them).
+ *   out (device) [batch][Hq][v_dim] in p->out_dtype.
+ */
+kvq_status kvq_decode(const kvq_cache* c, const kvq_decode_params* p, const void* q,
+                      float* part_o, float* part_lse, uint32_t* counters, void* out,
+                      void* stream);
 
 /*
  * Elementwise fp32 -> code conversions with the device encoders the append

@@ -81,7 +81,8 @@ kvq_status check_cache(const kvq_cache* c) {
 kvq_status check_params(const kvq_decode_params* p) {
   if (!p) return KVQ_ERR_INVALID;
   if (p->batch < 0 || p->num_q_heads < 1 || p->qk_dim < 1 || p->v_dim < 1) return KVQ_ERR_INVALID;
-  if (p->num_splits < 1 || p->num_splits > 4096) return KVQ_ERR_INVALID;
+  if (p->num_splits < 1) return KVQ_ERR_INVALID;
+  if (p->num_splits > kMaxFusedSplits) return KVQ_ERR_UNSUPPORTED;
   if (p->max_kv_len < 0) return KVQ_ERR_INVALID;
   if (p->batch > 0 && !p->seq_lens) return KVQ_ERR_INVALID;
   if (!finite_pos(p->sm_scale)) return KVQ_ERR_INVALID;
@@ -201,14 +202,22 @@ size_t kvq_partial_workspace_bytes(int batch, int num_q_heads, int num_splits, i
   return rows * (size_t)v_dim * sizeof(float) + rows * sizeof(float);
 }
 
-kvq_status kvq_decode_partial(const kvq_cache* c, const kvq_decode_params* p, const void* q,
-                              float* part_o, float* part_lse, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of kvq_decode_partial and kvq_decode (fused when counters).
+kvq_status decode_impl(const kvq_cache* c, const kvq_decode_params* p, const void* q,
+                       float* part_o, float* part_lse, uint32_t* counters, void* out,
+                       cudaStream_t stream) {
   kvq_status s = check_cache(c);
   if (s != KVQ_OK) return s;
   s = check_params(p);
   if (s != KVQ_OK) return s;
   if (p->batch == 0) return KVQ_OK;
-  if (!q || !aligned16(q) || !part_o || !part_lse) return KVQ_ERR_INVALID;
+  if (!q || !aligned16(q) || !part_o || !aligned16(part_o) || !part_lse) return KVQ_ERR_INVALID;
+  if (counters && !out) return KVQ_ERR_INVALID;
+  if (counters && p->num_splits > kMaxFusedSplits) return KVQ_ERR_UNSUPPORTED;
   if (p->num_q_heads % c->num_kv_heads != 0) return KVQ_ERR_INVALID;
   const int G = p->num_q_heads / c->num_kv_heads;
   if (G > kMaxGroup) return KVQ_ERR_UNSUPPORTED;
@@ -216,10 +225,12 @@ kvq_status kvq_decode_partial(const kvq_cache* c, const kvq_decode_params* p, co
     return KVQ_ERR_INVALID;
   if ((long long)p->batch * c->num_kv_heads >= (1LL << 31)) return KVQ_ERR_UNSUPPORTED;
   const bool probq = p->prob_scale > 0.f;
+  long long score_floats = 0;
   if (probq) {
     long long chunk = ((long long)p->max_kv_len + p->num_splits - 1) / p->num_splits;
     chunk = (chunk + 15) / 16 * 16;
-    if (chunk * G > kScoreCapacity) return KVQ_ERR_UNSUPPORTED;
+    score_floats = chunk * G;
+    if (score_floats > kScoreCapacity) return KVQ_ERR_UNSUPPORTED;
   }
   const int D = c->head_dim;
   const uint64_t rows = (uint64_t)c->num_pages * c->num_kv_heads * c->page_size;
@@ -243,8 +254,14 @@ kvq_status kvq_decode_partial(const kvq_cache* c, const kvq_decode_params* p, co
   a.num_pages = c->num_pages;
   a.num_splits = p->num_splits;
   a.max_kv_len = p->max_kv_len;
+  a.Dv = p->v_dim;
+  a.score_floats = (int)score_floats;
   a.qk_scale_log2 = p->sm_scale * c->k_scale * 1.4426950408889634f;
   a.prob_scale = p->prob_scale;
+  a.counters = counters;
+  a.out = out;
+  a.out_dtype = p->out_dtype;
+  a.out_scale = p->out_scale;
 
   if (is_mla(c)) {
     if (D != 512 || c->rope_dim != 64 || G != 16 || p->qk_dim != 576 || p->v_dim != 512)
@@ -253,7 +270,9 @@ kvq_status kvq_decode_partial(const kvq_cache* c, const kvq_decode_params* p, co
     a.out_mult = c->k_scale;   // the values are the latent itself
     CUtensorMap tk;
     if (!make_row_map(&tk, c->k_codes, D / 2, rows)) return KVQ_ERR_CUDA;
-    return cuda_status(launch_mla_partial(tk, a, as_stream(stream)));
+    cudaError_t e = launch_mla_partial(tk, a, stream);
+    if (e == cudaErrorNotSupported) return KVQ_ERR_UNSUPPORTED;
+    return cuda_status(e);
   }
   if (p->qk_dim != D || p->v_dim != D) return KVQ_ERR_INVALID;
   const bool ok_dims = (c->fmt == KVQ_FP8_E4M3 && (D == 64 || D == 128)) ||
@@ -265,7 +284,24 @@ kvq_status kvq_decode_partial(const kvq_cache* c, const kvq_decode_params* p, co
   if (!make_row_map(&maps.k16, c->k_codes, row_bytes, rows) ||
       !make_row_map(&maps.v16, c->v_codes, row_bytes, rows))
     return KVQ_ERR_CUDA;
-  return cuda_status(launch_partial(c->fmt, D, probq, maps, a, as_stream(stream)));
+  return cuda_status(launch_partial(c->fmt, D, probq, maps, a, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_decode_partial(const kvq_cache* c, const kvq_decode_params* p, const void* q,
+                              float* part_o, float* part_lse, void* stream) {
+  return decode_impl(c, p, q, part_o, part_lse, nullptr, nullptr, as_stream(stream));
+}
+
+kvq_status kvq_decode(const kvq_cache* c, const kvq_decode_params* p, const void* q,
+                      float* part_o, float* part_lse, uint32_t* counters, void* out,
+                      void* stream) {
+  if (p && p->batch > 0 && (!counters || !out)) return KVQ_ERR_INVALID;
+  return decode_impl(c, p, q, part_o, part_lse, counters ? counters : nullptr, out,
+                     as_stream(stream));
 }
 
 kvq_status kvq_decode_combine(const kvq_decode_params* p, const float* part_o,
@@ -273,8 +309,10 @@ kvq_status kvq_decode_combine(const kvq_decode_params* p, const float* part_o,
   kvq_status s = check_params(p);
   if (s != KVQ_OK) return s;
   if (p->batch == 0) return KVQ_OK;
-  if (!part_o || !part_lse || !out) return KVQ_ERR_INVALID;
+  if (!part_o || !aligned16(part_o) || !part_lse || !out || p->v_dim % 4 != 0)
+    return KVQ_ERR_INVALID;
   if ((long long)p->batch * p->num_q_heads >= (1LL << 31)) return KVQ_ERR_UNSUPPORTED;
+  if (p->num_splits > kMaxFusedSplits) return KVQ_ERR_UNSUPPORTED;
   CombineArgs a{};
   a.part_o = part_o;
   a.part_lse = part_lse;

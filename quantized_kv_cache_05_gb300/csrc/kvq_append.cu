@@ -40,6 +40,7 @@ __device__ __forceinline__ long cache_row(const AppendArgs& a, int b, int pos, i
 
 // grid.y = 0: K, 1: V (or the MLA rope keys)
 __global__ void __launch_bounds__(256) append_fp8_kernel(const AppendArgs a) {
+  griddep_launch_dependents();   // the decode kernel may launch now (it waits for us)
   const int per_row = a.D / 8;
   const size_t rows = (size_t)a.batch * a.T * a.Hkv;
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -86,6 +87,7 @@ __device__ __forceinline__ void nvfp4_block(const float* f, float g, uint32_t& w
 }
 
 __global__ void __launch_bounds__(256) append_nvfp4_kernel(const AppendArgs a) {
+  griddep_launch_dependents();   // the decode kernel may launch now (it waits for us)
   const int per_row = a.D / 16;
   const size_t rows = (size_t)a.batch * a.T * a.Hkv;
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -113,6 +115,7 @@ __global__ void __launch_bounds__(256) append_nvfp4_kernel(const AppendArgs a) {
 
 // MLA rope keys: plain bf16 copy into k_pe [page][ps][rope] (Hkv = 1).
 __global__ void __launch_bounds__(256) append_rope_kernel(const AppendArgs a) {
+  griddep_launch_dependents();   // the decode kernel may launch now (it waits for us)
   const int per_row = a.rope / 8;
   const size_t rows = (size_t)a.batch * a.T;
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;

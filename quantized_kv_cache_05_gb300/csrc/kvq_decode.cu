@@ -221,15 +221,105 @@ __device__ __forceinline__ int obuf_swz(int head, int d) {
   return d ^ ((((head >> 1) & 3) | ((grp >> (5 - kLog)) << 2)) & ((D / 8) - 1));
 }
 
-__device__ __forceinline__ float quad_max(float v) {
-  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-  return v;
+// Output of one element in the requested type: fp32, bf16 (round to nearest
+// even) or the E4M3 code of fl32(o / out_scale).
+__device__ __forceinline__ void store_out(void* out, int dtype, float out_scale, size_t i, float v) {
+  if (dtype == 0) {
+    static_cast<float*>(out)[i] = v;
+  } else if (dtype == 1) {
+    static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
+  } else {
+    static_cast<uint8_t*>(out)[i] = (uint8_t)(f32x2_to_e4m3x2(__fdiv_rn(v, out_scale), 0.f) & 0xFFu);
+  }
 }
-__device__ __forceinline__ float quad_sum(float v) {
-  v += __shfl_xor_sync(0xffffffffu, v, 1);
-  v += __shfl_xor_sync(0xffffffffu, v, 2);
-  return v;
+
+// Merge of the s split partials of `rows` consecutive query heads starting at
+// partial row `row0` (M = max lse, w_j = e^(lse_j - M), O = sum w_j o_j /
+// sum w_j; O = 0 when every split is empty), written to `out` in the
+// requested type.  One warp per head row computes the weights (warp
+// reductions); all threads then sum the partials with eight independent
+// loads in flight.  w: rows * kMaxFusedSplits floats of shared memory (s <=
+// kMaxFusedSplits), winv: rows floats.  The caller synchronizes before.
+__device__ __forceinline__ void merge_rows(const float* part_o, const float* part_lse,
+                                           size_t row0, int rows, int s, int Dv, float* w,
+                                           float* winv, void* out, int out_dtype,
+                                           float out_scale) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = warp; r < rows; r += blockDim.x >> 5) {
+    const float* lse = part_lse + (row0 + r) * s;
+    float lv[kMaxFusedSplits / 32];
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kMaxFusedSplits / 32; ++k) {
+      const int j = lane + 32 * k;
+      lv[k] = j < s ? __ldcg(lse + j) : -INFINITY;
+      M = fmaxf(M, lv[k]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxFusedSplits / 32; ++k) {
+      const int j = lane + 32 * k;
+      const float v = (M == -INFINITY || lv[k] == -INFINITY) ? 0.f : expf(lv[k] - M);
+      if (j < s) w[r * kMaxFusedSplits + j] = v;
+      sum += v;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) winv[r] = sum > 0.f ? 1.f / sum : (sum == 0.f ? 0.f : NAN);
+  }
+  __syncthreads();
+  // four consecutive value dims per thread (float4), sixteen splits in flight
+  const int nq = Dv / 4;
+  for (int i = threadIdx.x; i < rows * nq; i += blockDim.x) {
+    const int r = i / nq, d4 = i % nq;
+    const float4* po =
+        reinterpret_cast<const float4*>(part_o + (row0 + r) * (size_t)s * Dv) + d4;
+    const float* wr = w + r * kMaxFusedSplits;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 < s; j0 += 16) {
+      float4 v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        v[k] = j0 + k < s ? __ldcg(po + (size_t)(j0 + k) * nq) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float wk = j0 + k < s ? wr[j0 + k] : 0.f;
+        acc.x += wk * v[k].x;
+        acc.y += wk * v[k].y;
+        acc.z += wk * v[k].z;
+        acc.w += wk * v[k].w;
+      }
+    }
+    const float iv = winv[r];
+    const size_t o = (row0 + r) * Dv + 4 * d4;
+    store_out(out, out_dtype, out_scale, o + 0, acc.x * iv);
+    store_out(out, out_dtype, out_scale, o + 1, acc.y * iv);
+    store_out(out, out_dtype, out_scale, o + 2, acc.z * iv);
+    store_out(out, out_dtype, out_scale, o + 3, acc.w * iv);
+  }
+}
+
+// Fused combine: the last CTA of a (request, kv head) to finish merges the
+// s partials of its G query heads and writes the output; it then resets the
+// arrival counter for the next call.  wbuf: kMaxGroup * (kMaxFusedSplits + 1)
+// floats of shared memory.
+__device__ __forceinline__ void fused_combine(const PartialArgs& a, int bh, size_t part_row,
+                                              float* wbuf) {
+  __shared__ int is_last;
+  __threadfence();      // this CTA's partials are visible before it arrives
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(a.counters + bh, 1u);
+    is_last = prev == (unsigned)(a.num_splits - 1);
+    if (is_last) a.counters[bh] = 0u;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();      // ... and the other CTAs' partials before we read them
+  merge_rows(a.part_o, a.part_lse, part_row, a.G, a.num_splits, a.Dv, wbuf,
+             wbuf + kMaxGroup * kMaxFusedSplits, a.out, a.out_dtype, a.out_scale);
 }
 
 // NH = number of 8-head groups (1: up to 8 query heads per kv head, 2: up to 16)
@@ -254,6 +344,10 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
   // ring base, aligned for the 128-byte swizzle pattern
   const uint32_t ring = (smem_u32(dyn_smem) + 1023u) & ~1023u;
   const uint32_t scores = ring + Gm::kRing;   // FP8-prob mode only
+
+  // inputs may come from the previous kernel in the stream (launched with
+  // programmatic serialization, this kernel can start before it ends)
+  griddep_wait();
 
   // chunk of this split
   int L = a.seq_lens[b];
@@ -640,55 +734,32 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
     }
     a.part_o[((part_row + row) * a.num_splits + split) * D + d] = acc;
   }
+  if (a.counters) fused_combine(a, bh, part_row, obuf + kDecodeWarps * kMaxGroup * D);
 }
 
 // ---------------------------------------------------------------------------
-// Combine: one CTA per (request, query head).
+// Combine: one CTA merges kCombineRows consecutive (request, query head) rows.
 // ---------------------------------------------------------------------------
+constexpr int kCombineRows = 4;
+
 __global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
-  extern __shared__ float w[];   // num_splits weights
-  __shared__ float wsum_s;
-  const int row = blockIdx.x;
-  const float* lse = a.part_lse + (size_t)row * a.num_splits;
-  if (threadIdx.x < 32) {
-    float M = -INFINITY;
-    for (int j = threadIdx.x; j < a.num_splits; j += 32) M = fmaxf(M, lse[j]);
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float s = 0.f;
-    for (int j = threadIdx.x; j < a.num_splits; j += 32) {
-      const float v = (M == -INFINITY || lse[j] == -INFINITY) ? 0.f : expf(lse[j] - M);
-      w[j] = v;
-      s += v;
-    }
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (threadIdx.x == 0) wsum_s = s;
-  }
-  __syncthreads();
-  const float inv = wsum_s > 0.f ? 1.f / wsum_s : 0.f;
-  const float* po = a.part_o + (size_t)row * a.num_splits * a.Dv;
-  for (int d = threadIdx.x; d < a.Dv; d += blockDim.x) {
-    float acc = 0.f;
-    for (int j = 0; j < a.num_splits; ++j)
-      if (w[j] != 0.f) acc += w[j] * po[(size_t)j * a.Dv + d];
-    const float v = wsum_s > 0.f ? acc * inv : 0.f;
-    const size_t oi = (size_t)row * a.Dv + d;
-    if (a.out_dtype == 0) {
-      static_cast<float*>(a.out)[oi] = v;
-    } else if (a.out_dtype == 1) {
-      static_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(v);
-    } else {
-      static_cast<uint8_t*>(a.out)[oi] =
-          (uint8_t)(f32x2_to_e4m3x2(__fdiv_rn(v, a.out_scale), 0.f) & 0xFFu);
-    }
-  }
+  __shared__ float w[kCombineRows * kMaxFusedSplits];
+  __shared__ float winv[kCombineRows];
+  griddep_wait();
+  const size_t row0 = (size_t)blockIdx.x * kCombineRows;
+  const int rows = (int)min((size_t)kCombineRows, (size_t)a.rows - row0);
+  merge_rows(a.part_o, a.part_lse, row0, rows, a.num_splits, a.Dv, w, winv, a.out, a.out_dtype,
+             a.out_scale);
 }
 
 template <int FMT, int D, bool PROBQ, int NH>
 cudaError_t launch_partial_t(const TensorMaps& m, const PartialArgs& a, cudaStream_t st) {
   using Gm = Geom<FMT, D>;
-  static_assert((size_t)kDecodeWarps * kMaxGroup * D * 4 <= (size_t)Gm::kRing,
-                "the merge buffer must fit in the ring");
-  const size_t smem = 1024 + (size_t)Gm::kRing + (PROBQ ? (size_t)kScoreCapacity * 4 : 0);
+  static_assert((size_t)kDecodeWarps * kMaxGroup * D * 4 +
+                        (size_t)(kMaxGroup * kMaxFusedSplits + kMaxGroup) * 4 <=
+                    (size_t)Gm::kRing,
+                "the merge buffer and the combine weights must fit in the ring");
+  const size_t smem = 1024 + (size_t)Gm::kRing + (PROBQ ? (size_t)a.score_floats * 4 : 0);
   auto kern = partial_kernel<FMT, D, PROBQ, NH>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -696,9 +767,8 @@ cudaError_t launch_partial_t(const TensorMaps& m, const PartialArgs& a, cudaStre
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.batch * a.Hkv, a.num_splits);
-  kern<<<grid, kDecodeThreads, smem, st>>>(m.k16, m.v16, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(a.batch * a.Hkv, a.num_splits), dim3(kDecodeThreads), smem, st,
+                    m.k16, m.v16, a);
 }
 
 template <int FMT, int D>
@@ -721,8 +791,9 @@ cudaError_t launch_partial(int fmt, int D, bool probq, const TensorMaps& m, cons
 }
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
-  combine_kernel<<<a.rows, 128, (size_t)a.num_splits * sizeof(float), st>>>(a);
-  return cudaGetLastError();
+  if (a.num_splits > kMaxFusedSplits) return cudaErrorInvalidValue;
+  return launch_pdl(combine_kernel, dim3((a.rows + kCombineRows - 1) / kCombineRows), dim3(128),
+                    0, st, a);
 }
 
 }  // namespace kvq

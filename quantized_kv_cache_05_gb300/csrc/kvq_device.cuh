@@ -247,6 +247,16 @@ __device__ __forceinline__ uint32_t lds8(uint32_t addr) {
   return v;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream runs; it
+// must wait here before reading anything that kernel produces.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next (programmatically serialized) kernel in the stream launch.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void record_error(int32_t* flag, int bits) {
   if (flag) atomicOr(flag, bits);
 }

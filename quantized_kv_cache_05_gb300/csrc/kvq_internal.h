@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <utility>
 
 namespace kvq {
 
@@ -19,7 +20,8 @@ constexpr int kDecodeThreads = 32 * kDecodeWarps;
 constexpr int kStages = 4;        // boxes in flight per warp
 constexpr int kMaxGroup = 16;     // query heads per kv head (two 8-head MMA tiles)
 constexpr int kScoreCapacity = 16384;  // fp32 scores per CTA in FP8-prob mode
-constexpr int kPageCache = 1024;  // block-table entries of a chunk kept in shared memory
+constexpr int kPageCache = 512;   // block-table entries of a chunk kept in shared memory
+constexpr int kMaxFusedSplits = 64;  // splits the fused decode merges in one CTA
 
 struct AppendArgs {
   int fmt, D, Hkv, ps, max_pages, batch, T, rope, num_pages;
@@ -48,9 +50,16 @@ struct PartialArgs {
   float* part_lse;
   int32_t* error_flag;
   int batch, Hq, Hkv, G, ps, max_pages, num_splits, max_kv_len, num_pages;
+  int Dv;                     // value dim (the partials' row length)
+  int score_floats;           // FP8-prob mode: scores one chunk needs (<= kScoreCapacity)
   float qk_scale_log2;        // sm_scale * k_scale * log2(e)
   float out_mult;             // v_scale (times prob_scale with FP8 probabilities)
   float prob_scale;           // > 0: FP8 probabilities
+  // fused combine (kvq_decode): arrival counters [B * Hkv] and the output
+  uint32_t* counters;         // null: partials only
+  void* out;
+  int out_dtype;
+  float out_scale;
 };
 
 struct CombineArgs {
@@ -60,6 +69,24 @@ struct CombineArgs {
   int rows, num_splits, Dv, out_dtype;
   float out_scale;
 };
+
+// Launch with programmatic stream serialization (the kernel calls
+// griddep_wait() before reading its inputs).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_amax_bf16(const uint16_t* x, size_t n, float* out, cudaStream_t st);

@@ -59,6 +59,8 @@ SIGNATURES = {
     "kvq_decode_partial": (_int, [ctypes.POINTER(kvq_cache), ctypes.POINTER(kvq_decode_params),
                                   _P, _P, _P, _P]),
     "kvq_decode_combine": (_int, [ctypes.POINTER(kvq_decode_params), _P, _P, _P, _P]),
+    "kvq_decode": (_int, [ctypes.POINTER(kvq_cache), ctypes.POINTER(kvq_decode_params), _P, _P,
+                          _P, _P, _P, _P]),
     "kvq_encode_e4m3": (_int, [_P, _P, _sz, _P]),
     "kvq_encode_e2m1": (_int, [_P, _P, _sz, _P]),
 }
@@ -167,6 +169,12 @@ def kvq_decode_partial(cache: kvq_cache, params: kvq_decode_params, q, part_o, p
 def kvq_decode_combine(params: kvq_decode_params, part_o, part_lse, out, stream=None) -> int:
     return lib().kvq_decode_combine(_ref(params), _addr(part_o), _addr(part_lse),
                                     _addr(out), _stream(stream))
+
+
+def kvq_decode(cache: kvq_cache, params: kvq_decode_params, q, part_o, part_lse, counters,
+               out, stream=None) -> int:
+    return lib().kvq_decode(_ref(cache), _ref(params), _addr(q), _addr(part_o), _addr(part_lse),
+                            _addr(counters), _addr(out), _stream(stream))
 
 
 def kvq_encode_e4m3(x, out, n: int, stream=None) -> int:

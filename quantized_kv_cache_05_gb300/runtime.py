@@ -115,6 +115,26 @@ class DecodeWorkspace:
                                device=device)
 
 
+class FusedWorkspace(DecodeWorkspace):
+    """Scratch of kvq_decode: split partials plus arrival counters, which are
+    zeroed once here; every call leaves them at zero again."""
+
+    def __init__(self, cfg: DecodeConfig, num_kv_heads: int, device="cuda"):
+        super().__init__(cfg, device)
+        self.counters = torch.zeros(cfg.batch * num_kv_heads, dtype=torch.int32, device=device)
+
+
+def decode_fused(cache: QuantizedKVCache, q: torch.Tensor, seq_lens: torch.Tensor,
+                 cfg: DecodeConfig, ws: Optional[FusedWorkspace] = None,
+                 error_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One decode step in one launch (kvq_decode)."""
+    ws = ws or FusedWorkspace(cfg, cache.Hkv, q.device)
+    p = cfg.params(seq_lens, error_flag)
+    kvq.check(kvq.kvq_decode(cache.struct(), p, q, ws.part_o, ws.part_lse, ws.counters, ws.out,
+                             stream), "kvq_decode")
+    return ws.out
+
+
 def auto_splits(batch: int, num_kv_heads: int, q_per_kv: int, max_kv_len: int, fmt: str,
                 device: int | None = None) -> int:
     if device is None:

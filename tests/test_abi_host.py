@@ -188,3 +188,17 @@ def test_misc_rejects(L):
     assert kvq.kvq_encode_e4m3(None, 0x1000, 4, None) == kvq.KVQ_ERR_INVALID
     assert kvq.kvq_encode_e2m1(0x1000, None, 4, None) == kvq.KVQ_ERR_INVALID
     assert kvq.kvq_encode_e4m3(None, None, 0, None) == kvq.KVQ_OK
+
+
+def test_fused_decode_rejects(L):
+    c, p = good_cache(), good_params()
+    f = kvq.kvq_decode
+    assert f(c, p, 0x50000, 0x60000, 0x70000, None, 0x80000, None) == kvq.KVQ_ERR_INVALID
+    assert f(c, p, 0x50000, 0x60000, 0x70000, 0x90000, None, None) == kvq.KVQ_ERR_INVALID
+    assert f(c, p, 0x50000, None, 0x70000, 0x90000, 0x80000, None) == kvq.KVQ_ERR_INVALID
+    p.num_splits = 65
+    assert f(c, p, 0x50000, 0x60000, 0x70000, 0x90000, 0x80000, None) == kvq.KVQ_ERR_UNSUPPORTED
+    assert kvq.kvq_decode_partial(c, p, 0x50000, 0x60000, 0x70000, None) == kvq.KVQ_ERR_UNSUPPORTED
+    assert kvq.kvq_decode_combine(p, 0x60000, 0x70000, 0x80000, None) == kvq.KVQ_ERR_UNSUPPORTED
+    p.num_splits, p.batch = 2, 0
+    assert f(c, p, None, None, None, None, None, None) == kvq.KVQ_OK
