@@ -64,7 +64,7 @@ def hbm_peak():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ["kvq_decode.cu", "kvq_device.cuh", "kvq_internal.h"]:
+    for f in ["kvq_decode.cu", "kvq_attn.cuh", "kvq_device.cuh", "kvq_internal.h"]:
         with open(os.path.join(ROOT, "quantized_kv_cache_05_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -139,6 +139,18 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest per-rank value (the job's time is its slowest replica).  Works
+    with NCCL (device tensor) and gloo (CPU tensor)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 # ---------------------------------------------------------------------------
@@ -350,11 +362,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    us = statistics.mean(step_us)
-    if world > 1:
-        t = torch.tensor([us], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        us = float(t.item())
+    us = max_over_ranks(statistics.mean(step_us), device)
     e2e_us, bi, bo = bench.e2e(max(10, args.steps // 2), args.warmup)
     part = statistics.mean(part_us)
     achieved = bench.partial_bytes() / (part * 1e-6) / 1e9

@@ -1,0 +1,280 @@
+// Device-side pieces shared by the split-KV decode kernels (GQA/MHA and
+// MLA): ring geometry, register-level fragment decoders for the tensor-core
+// operands, bounded barrier waits, and the merge of split partials.
+#pragma once
+
+#include <cmath>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLazyMax = 8.0f;   // log2 headroom before the running max moves
+
+template <int FMT, int D>
+struct Geom {
+  static constexpr int kRow = FMT == kFmtFp8 ? D : D / 2;   // code bytes per token row
+  static constexpr int kSRow = FMT == kFmtFp8 ? 0 : D / 16; // scale bytes per token row
+  static constexpr int kBoxK = kBoxTokens * kRow;            // code bytes of one box
+  static constexpr int kBoxS = kBoxTokens * kSRow;           // scale bytes of one box
+  // one ring stage: [K codes][V codes][K scales][V scales], padded so that
+  // every stage starts on the 1024-byte swizzle period
+  static constexpr int kStage = (2 * (kBoxK + kBoxS) + 1023) / 1024 * 1024;
+  static constexpr int kRing = kDecodeWarps * kStages * kStage;
+  static constexpr int kKSteps = D / 16;   // QK k-steps over head_dim
+  static constexpr int kMT = D / 16;       // PV m-tiles over v_dim
+  // physical 16-byte chunk of logical chunk `ch` in row `row` of a box
+  __device__ static __forceinline__ int swz(int row, int ch) {
+    if constexpr (kRow == 128) return ch ^ (row & 7);
+    else return ch ^ ((row >> 1) & 3);                        // 64-byte rows
+  }
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > 250000000ull || i > (1u << 28)) return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K fragments (B operand of S = Q K^T) for one 8-token n-tile: b[j][0..1] for
+// k-step j.  Lane (g, t) holds token row `row` (= 8u + g) and head dims
+//   d = (D/4) t + 4 j + {0, 1} (b[j][0]) and + {2, 3} (b[j][1]).
+// ---------------------------------------------------------------------------
+template <int FMT, int D, int SSTRIDE = Geom<FMT, D>::kSRow>
+__device__ __forceinline__ void k_frag(uint32_t boxK, uint32_t boxKs, int row, int t,
+                                       uint32_t (&b)[D / 16][2]) {
+  using Gm = Geom<FMT, D>;
+  if constexpr (FMT == kFmtFp8) {
+    constexpr int NCH = D / 64;  // 16-byte chunks per lane per row
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      uint4 v = lds128(boxK + row * Gm::kRow + (Gm::swz(row, t * NCH + i) << 4));
+      e4m3x4_to_f16x2x2(v.x, b[i * 4 + 0][0], b[i * 4 + 0][1]);
+      e4m3x4_to_f16x2x2(v.y, b[i * 4 + 1][0], b[i * 4 + 1][1]);
+      e4m3x4_to_f16x2x2(v.z, b[i * 4 + 2][0], b[i * 4 + 2][1]);
+      e4m3x4_to_f16x2x2(v.w, b[i * 4 + 3][0], b[i * 4 + 3][1]);
+    }
+  } else {
+    static_assert(D == 128, "NVFP4 decode supports head_dim 128");
+    uint4 v = lds128(boxK + row * Gm::kRow + (Gm::swz(row, t) << 4));
+    uint32_t sc = lds16(boxKs + row * SSTRIDE + 2 * t);   // blocks 2t, 2t+1
+    uint32_t s2 = e4m3x2_to_f16x2(sc);
+    uint32_t s_lo = __byte_perm(s2, 0, 0x1010), s_hi = __byte_perm(s2, 0, 0x3232);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t o0, o1, o2, o3;
+      e2m1x8_to_f16x2x4(w[k], o0, o1, o2, o3);
+      uint32_t s = k < 2 ? s_lo : s_hi;
+      b[2 * k][0] = hmul2(o0, s);
+      b[2 * k][1] = hmul2(o1, s);
+      b[2 * k + 1][0] = hmul2(o2, s);
+      b[2 * k + 1][1] = hmul2(o3, s);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// V^T fragments (A operand of O^T = V^T P^T) for the box's 16 tokens:
+// a[i][0..3] for m-tile i.  Lane (g, t) covers tokens 2t, 2t+1 (a0, a1) and
+// 2t+8, 2t+9 (a2, a3); m-tile i, row g is value dim (D/8) g + 2 i and row
+// g + 8 is (D/8) g + 2 i + 1.  Invalid tokens read as zero codes.
+// ---------------------------------------------------------------------------
+template <int FMT, int D, int SSTRIDE = Geom<FMT, D>::kSRow>
+__device__ __forceinline__ void v_frag(uint32_t boxV, uint32_t boxVs, int t, int g, int nvalid,
+                                       uint32_t (&a)[D / 16][4]) {
+  using Gm = Geom<FMT, D>;
+  const int tk[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+  if constexpr (FMT == kFmtFp8) {
+    constexpr int NW = D / 32;   // words per lane per token (4 for D=128, 2 for D=64)
+    uint32_t w[4][NW];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      if constexpr (D == 128) {
+        uint4 v = lds128(boxV + tk[r] * 128 + (Gm::swz(tk[r], g) << 4));
+        w[r][0] = v.x; w[r][1] = v.y; w[r][2] = v.z; w[r][3] = v.w;
+      } else {
+        uint2 v = lds64(boxV + tk[r] * 64 + (Gm::swz(tk[r], g >> 1) << 4) + ((g & 1) << 3));
+        w[r][0] = v.x; w[r][1] = v.y;
+      }
+      if (tk[r] >= nvalid) {
+#pragma unroll
+        for (int k = 0; k < NW; ++k) w[r][k] = 0u;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < NW; ++k) {
+      // token pairs (2t, 2t+1) and (2t+8, 2t+9), one byte of each per value dim
+      const uint32_t p0 = __byte_perm(w[0][k], w[1][k], 0x5140);
+      const uint32_t p1 = __byte_perm(w[0][k], w[1][k], 0x7362);
+      const uint32_t q0 = __byte_perm(w[2][k], w[3][k], 0x5140);
+      const uint32_t q1 = __byte_perm(w[2][k], w[3][k], 0x7362);
+      e4m3x4_to_f16x2x2(p0, a[2 * k][0], a[2 * k][1]);
+      e4m3x4_to_f16x2x2(q0, a[2 * k][2], a[2 * k][3]);
+      e4m3x4_to_f16x2x2(p1, a[2 * k + 1][0], a[2 * k + 1][1]);
+      e4m3x4_to_f16x2x2(q1, a[2 * k + 1][2], a[2 * k + 1][3]);
+    }
+  } else {
+    static_assert(FMT == kFmtNvfp4 && D == 128, "unsupported V layout");
+    // 16 elements per token: bytes [8g, 8g+8) of the 64-byte row, block g
+    uint2 v[4];
+    uint32_t sc[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      v[r] = lds64(boxV + tk[r] * 64 + (Gm::swz(tk[r], g >> 1) << 4) + ((g & 1) << 3));
+      sc[r] = lds8(boxVs + tk[r] * SSTRIDE + g);
+      if (tk[r] >= nvalid) {
+        v[r] = make_uint2(0, 0);
+        sc[r] = 0;
+      }
+    }
+    const uint32_t s01 = e4m3x2_to_f16x2(sc[0] | (sc[1] << 8));   // (scale_2t, scale_2t+1)
+    const uint32_t s89 = e4m3x2_to_f16x2(sc[2] | (sc[3] << 8));
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t A = k ? v[0].y : v[0].x, B = k ? v[1].y : v[1].x;
+      const uint32_t C = k ? v[2].y : v[2].x, E = k ? v[3].y : v[3].x;
+      const uint32_t evAB = (A & 0x0F0F0F0Fu) | ((B & 0x0F0F0F0Fu) << 4);
+      const uint32_t odAB = ((A >> 4) & 0x0F0F0F0Fu) | (B & 0xF0F0F0F0u);
+      const uint32_t evCE = (C & 0x0F0F0F0Fu) | ((E & 0x0F0F0F0Fu) << 4);
+      const uint32_t odCE = ((C >> 4) & 0x0F0F0F0Fu) | (E & 0xF0F0F0F0u);
+      uint32_t e[4], o[4], f[4], h[4];
+      e2m1x8_to_f16x2x4(evAB, e[0], e[1], e[2], e[3]);
+      e2m1x8_to_f16x2x4(odAB, o[0], o[1], o[2], o[3]);
+      e2m1x8_to_f16x2x4(evCE, f[0], f[1], f[2], f[3]);
+      e2m1x8_to_f16x2x4(odCE, h[0], h[1], h[2], h[3]);
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        const int i = 4 * k + bb;   // value dims (D/8) g + 8k + 2bb (+1)
+        a[i][0] = hmul2(e[bb], s01);
+        a[i][1] = hmul2(o[bb], s01);
+        a[i][2] = hmul2(f[bb], s89);
+        a[i][3] = hmul2(h[bb], s89);
+      }
+    }
+  }
+}
+
+// Column swizzle of the end-of-chunk O buffer [warp][head][d]: XOR-ing the
+// low bits of d with (head pair, high bits of the lane group) makes both the
+// fragment stores and the row-wise merge reads conflict-free.
+template <int D>
+__device__ __forceinline__ int obuf_swz(int head, int d) {
+  constexpr int kLog = D == 128 ? 4 : 3;   // log2(D / 8): dims per lane group
+  const int grp = d >> kLog;
+  return d ^ ((((head >> 1) & 3) | ((grp >> (5 - kLog)) << 2)) & ((D / 8) - 1));
+}
+
+// Output of one element in the requested type: fp32, bf16 (round to nearest
+// even) or the E4M3 code of fl32(o / out_scale).
+__device__ __forceinline__ void store_out(void* out, int dtype, float out_scale, size_t i, float v) {
+  if (dtype == 0) {
+    static_cast<float*>(out)[i] = v;
+  } else if (dtype == 1) {
+    static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
+  } else {
+    static_cast<uint8_t*>(out)[i] = (uint8_t)(f32x2_to_e4m3x2(__fdiv_rn(v, out_scale), 0.f) & 0xFFu);
+  }
+}
+
+// Merge of the s split partials of `rows` consecutive query heads starting at
+// partial row `row0` (M = max lse, w_j = e^(lse_j - M), O = sum w_j o_j /
+// sum w_j; O = 0 when every split is empty), written to `out` in the
+// requested type.  One warp per head row computes the weights (warp
+// reductions); all threads then sum the partials with eight independent
+// loads in flight.  w: rows * kMaxFusedSplits floats of shared memory (s <=
+// kMaxFusedSplits), winv: rows floats.  The caller synchronizes before.
+__device__ __forceinline__ void merge_rows(const float* part_o, const float* part_lse,
+                                           size_t row0, int rows, int s, int Dv, float* w,
+                                           float* winv, void* out, int out_dtype,
+                                           float out_scale) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = warp; r < rows; r += blockDim.x >> 5) {
+    const float* lse = part_lse + (row0 + r) * s;
+    float lv[kMaxFusedSplits / 32];
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kMaxFusedSplits / 32; ++k) {
+      const int j = lane + 32 * k;
+      lv[k] = j < s ? __ldcg(lse + j) : -INFINITY;
+      M = fmaxf(M, lv[k]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxFusedSplits / 32; ++k) {
+      const int j = lane + 32 * k;
+      const float v = (M == -INFINITY || lv[k] == -INFINITY) ? 0.f : expf(lv[k] - M);
+      if (j < s) w[r * kMaxFusedSplits + j] = v;
+      sum += v;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) winv[r] = sum > 0.f ? 1.f / sum : (sum == 0.f ? 0.f : NAN);
+  }
+  __syncthreads();
+  // four consecutive value dims per thread (float4), sixteen splits in flight
+  const int nq = Dv / 4;
+  for (int i = threadIdx.x; i < rows * nq; i += blockDim.x) {
+    const int r = i / nq, d4 = i % nq;
+    const float4* po =
+        reinterpret_cast<const float4*>(part_o + (row0 + r) * (size_t)s * Dv) + d4;
+    const float* wr = w + r * kMaxFusedSplits;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 < s; j0 += 16) {
+      float4 v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        v[k] = j0 + k < s ? __ldcg(po + (size_t)(j0 + k) * nq) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float wk = j0 + k < s ? wr[j0 + k] : 0.f;
+        acc.x += wk * v[k].x;
+        acc.y += wk * v[k].y;
+        acc.z += wk * v[k].z;
+        acc.w += wk * v[k].w;
+      }
+    }
+    const float iv = winv[r];
+    const size_t o = (row0 + r) * Dv + 4 * d4;
+    store_out(out, out_dtype, out_scale, o + 0, acc.x * iv);
+    store_out(out, out_dtype, out_scale, o + 1, acc.y * iv);
+    store_out(out, out_dtype, out_scale, o + 2, acc.z * iv);
+    store_out(out, out_dtype, out_scale, o + 3, acc.w * iv);
+  }
+}
+
+// Fused combine: the last CTA of a (request, kv head) to finish merges the
+// s partials of its G query heads and writes the output; it then resets the
+// arrival counter for the next call.  wbuf: kMaxGroup * (kMaxFusedSplits + 1)
+// floats of shared memory.
+__device__ __forceinline__ void fused_combine(const PartialArgs& a, int bh, size_t part_row,
+                                              float* wbuf) {
+  __shared__ int is_last;
+  __threadfence();      // this CTA's partials are visible before it arrives
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(a.counters + bh, 1u);
+    is_last = prev == (unsigned)(a.num_splits - 1);
+    if (is_last) a.counters[bh] = 0u;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();      // ... and the other CTAs' partials before we read them
+  merge_rows(a.part_o, a.part_lse, part_row, a.G, a.num_splits, a.Dv, wbuf,
+             wbuf + kMaxGroup * kMaxFusedSplits, a.out, a.out_dtype, a.out_scale);
+}
+
+
+}  // namespace kvq
