@@ -51,6 +51,21 @@ bool make_row_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D byte view [rows][n_slices][slice_bytes] of a row-major tensor whose rows
+// are n_slices * slice_bytes wide; boxes of one slice x 16 rows.
+bool make_slice_map(CUtensorMap* m, const void* base, uint64_t slice_bytes, uint64_t n_slices,
+                    uint64_t rows, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {slice_bytes, n_slices, rows};
+  cuuint64_t strides[2] = {slice_bytes, slice_bytes * n_slices};
+  cuuint32_t box[3] = {(cuuint32_t)slice_bytes, 1, (cuuint32_t)kBoxTokens};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool is_mla(const kvq_cache* c) { return c->rope_dim > 0; }
 
 // Checks shared by append and decode.
@@ -268,11 +283,14 @@ kvq_status decode_impl(const kvq_cache* c, const kvq_decode_params* p, const voi
       return KVQ_ERR_UNSUPPORTED;
     if (probq) return KVQ_ERR_UNSUPPORTED;
     a.out_mult = c->k_scale;   // the values are the latent itself
-    CUtensorMap tk;
-    if (!make_row_map(&tk, c->k_codes, D / 2, rows)) return KVQ_ERR_CUDA;
-    cudaError_t e = launch_mla_partial(tk, a, stream);
-    if (e == cudaErrorNotSupported) return KVQ_ERR_UNSUPPORTED;
-    return cuda_status(e);
+    a.pe_scale_log2 = p->sm_scale * 1.4426950408889634f;
+    // four warps, each one 128-dim slice of the latent (64 code bytes) and a
+    // 16-dim slice of the rope key (32 bytes)
+    CUtensorMap tkv, tpe;
+    if (!make_slice_map(&tkv, c->k_codes, 64, 4, rows, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_slice_map(&tpe, c->k_pe, 32, 4, rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return KVQ_ERR_CUDA;
+    return cuda_status(launch_mla_partial(tkv, tpe, a, stream));
   }
   if (p->qk_dim != D || p->v_dim != D) return KVQ_ERR_INVALID;
   const bool ok_dims = (c->fmt == KVQ_FP8_E4M3 && (D == 64 || D == 128)) ||

@@ -53,6 +53,7 @@ struct PartialArgs {
   int Dv;                     // value dim (the partials' row length)
   int score_floats;           // FP8-prob mode: scores one chunk needs (<= kScoreCapacity)
   float qk_scale_log2;        // sm_scale * k_scale * log2(e)
+  float pe_scale_log2;        // MLA rope part: sm_scale * log2(e)
   float out_mult;             // v_scale (times prob_scale with FP8 probabilities)
   float prob_scale;           // > 0: FP8 probabilities
   // fused combine (kvq_decode): arrival counters [B * Hkv] and the output
@@ -98,7 +99,8 @@ struct TensorMaps {
 
 cudaError_t launch_partial(int fmt, int D, bool probq, const TensorMaps& m, const PartialArgs& a,
                            cudaStream_t st);
-cudaError_t launch_mla_partial(const CUtensorMap& tk, const PartialArgs& a, cudaStream_t st);
+cudaError_t launch_mla_partial(const CUtensorMap& tkv, const CUtensorMap& tpe,
+                               const PartialArgs& a, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 
 }  // namespace kvq

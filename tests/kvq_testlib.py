@@ -4,7 +4,7 @@ ABI) and in the oracle, plus the comparison rules.
 Comparison rules (floating point):
   * fp32 output: max |gpu - oracle| <= 2e-3 and cosine >= 0.9999 over the
     whole output;
-  * bf16 output: within one bf16 step of bf16_rne(oracle);
+  * bf16 output: within one bf16 step of bf16_rne(oracle), or within 2e-3;
   * E4M3 output: codes equal, or one code step apart where the oracle's
     pre-rounding value lies within 1e-3 (relative) of the rounding midpoint.
 Integer / byte work (codes, block scales) must be bit-exact.
@@ -185,11 +185,15 @@ def _bf16_ordered(bits: np.ndarray) -> np.ndarray:
 
 
 def assert_bf16_close(gpu_bits: np.ndarray, ref: np.ndarray, what: str = ""):
+    """Within one bf16 step of bf16_rne(oracle), or within the fp32 absolute
+    tolerance (near zero a sign flip of a tiny value is many steps)."""
     m = ~np.isnan(ref)
     rb = synth.f32_to_bf16(ref[m].astype(np.float32))
     d = np.abs(_bf16_ordered(gpu_bits[m]) - _bf16_ordered(rb))
-    assert d.max(initial=0) <= 1, f"{what}: bf16 outputs {d.max()} steps from the oracle"
-    return int((d == 1).sum())
+    gv = synth.bf16_to_f32(gpu_bits[m]).astype(np.float64)
+    ok = (d <= 1) | (np.abs(gv - ref[m]) <= F32_ATOL)
+    assert ok.all(), f"{what}: {int((~ok).sum())} bf16 outputs off (max {d[~ok].max()} steps)"
+    return int((d >= 1).sum())
 
 
 def assert_e4m3_close(gpu_codes: np.ndarray, ref: np.ndarray, out_scale: float, what=""):

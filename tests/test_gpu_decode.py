@@ -240,3 +240,62 @@ def test_fused_workspace_reuse_across_split_counts(gqa):
         a, _ = gqa.gpu_decode(s)
         b, _ = fused(gqa, s, ws=big)
         assert torch.allclose(a, b, rtol=4e-7, atol=1e-7), s
+
+
+# --------------------------------------------------------------------------
+# MLA: 16 heads on one NVFP4 latent cache + bf16 rope keys
+# --------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def mla():
+    w = synth.mla_nvfp4(B=3, L=300)
+    w.seq_lens = np.array([300, 37, 161], np.int32)
+    return Setup(w)
+
+
+@pytest.mark.parametrize("s", [1, 2, 5])
+def test_mla_two_launch(mla, s):
+    ref, _ = mla.oracle_decode()
+    out, _ = mla.gpu_decode(s)
+    assert_f32_close(out.cpu().numpy(), ref, f"mla s={s}")
+
+
+@pytest.mark.parametrize("s", [1, 4])
+def test_mla_fused(mla, s):
+    ref, _ = mla.oracle_decode()
+    out, ws = fused(mla, s)
+    assert_f32_close(out.cpu().numpy(), ref, f"mla fused s={s}")
+    assert not ws.counters.any()
+
+
+def test_mla_paged_bf16_out():
+    w = synth.mla_nvfp4(B=2, L=200)
+    w.seq_lens = np.array([200, 129], np.int32)
+    w.page_size = 16
+    w.permute_pages = True
+    S = Setup(w)
+    ref, _ = S.oracle_decode()
+    for s in (1, 3):
+        out, _ = S.gpu_decode(s, "bf16")
+        assert_bf16_close(bf16_bits(out), ref, f"mla paged bf16 s={s}")
+
+
+def test_mla_partials_per_chunk(mla):
+    s = 3
+    w = mla.w
+    _, ws = mla.gpu_decode(s)
+    po = ws.part_o.cpu().numpy().reshape(w.B, w.Hq, s, w.Dv)
+    pl = ws.part_lse.cpu().numpy().reshape(w.B, w.Hq, s)
+    q = mla.q64()
+    for b in range(w.B):
+        kh, vh = mla.oracle_kv(b, 0)
+        L = int(w.seq_lens[b])
+        for j in range(s):
+            st, en = oracle.chunk(L, s, j)
+            for hq in (0, 7, 15):
+                o, l = oracle.attention_partial(q[b, hq], kh, vh, st, en, w.sm_scale)
+                if en == st:
+                    assert np.isneginf(pl[b, hq, j]) and not po[b, hq, j].any()
+                    continue
+                assert abs(pl[b, hq, j] - l) <= 1e-4 * max(1.0, abs(l)), (b, hq, j)
+                assert_f32_close(po[b, hq, j], o, f"mla partial b{b} h{hq} j{j}")
