@@ -228,6 +228,30 @@ kvq_status kvq_decode(const kvq_cache* c, const kvq_decode_params* p, const void
                       void* stream);
 
 /*
+ * Allocation-free decode step (the paper has no counterpart; this is a
+ * convenience of this library).  For callers that cannot allocate device
+ * memory -- their device memory is owned by a host framework's fixed pool,
+ * or a hard memory budget forbids another cudaMalloc -- this does what
+ * kvq_decode does, but keeps the split partials and arrival counters in a
+ * static device buffer inside the library: KVQ_NOALLOC_SCRATCH_BYTES (4 MiB)
+ * that every GPU loading the library holds until the process exits.  The
+ * caller passes only inputs and the output.
+ *   Needs 256-aligned (4 * batch * num_kv_heads) + 256-aligned
+ *   (4 * batch * Hq * num_splits) + 4 * batch * Hq * num_splits * v_dim
+ *   bytes <= KVQ_NOALLOC_SCRATCH_BYTES; larger requests return
+ *   KVQ_ERR_WORKSPACE (use kvq_decode with caller-owned buffers).
+ *   The first call on a device looks up the buffer's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Every call clears the counters (an asynchronous memset on `stream`)
+ *   and then launches the decode; it allocates and frees nothing.
+ *   All calls share the one buffer: calls that overlap on the GPU (other
+ *   streams, other host threads) race and must be serialized by the caller.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (4u << 20)
+kvq_status kvq_decode_noalloc(const kvq_cache* c, const kvq_decode_params* p, const void* q,
+                              void* out, void* stream);
+
+/*
  * Elementwise fp32 -> code conversions with the device encoders the append
  * path uses: out[i] = E4M3(x[i]) (round to nearest even, saturating at
  * +-448) or the E2M1 nibble of x[i] (saturating at +-6) in the low 4 bits.

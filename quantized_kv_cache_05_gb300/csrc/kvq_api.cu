@@ -344,3 +344,71 @@ kvq_status kvq_decode_combine(const kvq_decode_params* p, const float* part_o,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode.
+//
+// Some callers cannot allocate device memory for the split partials: their
+// device memory is owned by a host framework that hands out only the tensors
+// it planned (a serving engine's fixed memory pool), or they run under a hard
+// memory budget where an extra cudaMalloc is not allowed.  kvq_decode_noalloc
+// serves them from one buffer the library itself carries: a file-scope device
+// array of KVQ_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds
+// until the process exits.  In host code the array's name is only a stand-in
+// for the symbol, so each device's real address is looked up once with
+// cudaGetSymbolAddress (with that device current) and passed to the kernel.
+// ---------------------------------------------------------------------------
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of this device's scratch array (looked up on first use).
+kvq_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return KVQ_ERR_CUDA;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return KVQ_OK;
+}
+
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" kvq_status kvq_decode_noalloc(const kvq_cache* c, const kvq_decode_params* p,
+                                         const void* q, void* out, void* stream) {
+  kvq_status st = check_cache(c);
+  if (st != KVQ_OK) return st;
+  st = check_params(p);
+  if (st != KVQ_OK) return st;
+  if (p->batch == 0) return KVQ_OK;
+  if (!q || !out) return KVQ_ERR_INVALID;
+  // scratch layout: [arrival counters][partial lse][partial o], 256-byte aligned
+  const size_t rows = (size_t)p->batch * p->num_q_heads * p->num_splits;
+  const size_t counter_bytes = up256((size_t)p->batch * c->num_kv_heads * sizeof(uint32_t));
+  const size_t lse_bytes = up256(rows * sizeof(float));
+  const size_t o_bytes = rows * (size_t)p->v_dim * sizeof(float);
+  if (counter_bytes + lse_bytes + o_bytes > KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;
+  void* base = nullptr;
+  st = noalloc_scratch(&base);
+  if (st != KVQ_OK) return st;
+  uint8_t* w = static_cast<uint8_t*>(base);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(w);
+  float* part_lse = reinterpret_cast<float*>(w + counter_bytes);
+  float* part_o = reinterpret_cast<float*>(w + counter_bytes + lse_bytes);
+  // the arrival counters must start at zero (a previous call leaves them
+  // zero; clearing them here keeps the contract independent of history)
+  if (cudaMemsetAsync(counters, 0, counter_bytes, as_stream(stream)) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  return decode_impl(c, p, q, part_o, part_lse, counters, out, as_stream(stream));
+}

@@ -23,6 +23,7 @@ KVQ_OK, KVQ_ERR_INVALID, KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA = 
 KVQ_FP8_E4M3, KVQ_NVFP4 = 1, 2
 KVQ_OUT_F32, KVQ_OUT_BF16, KVQ_OUT_E4M3 = 0, 1, 2
 KVQ_DEVERR_WAIT_TIMEOUT, KVQ_DEVERR_SEQ_CLAMPED = 1, 2
+KVQ_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _i32 = ctypes.c_int32
 _int = ctypes.c_int
@@ -61,6 +62,8 @@ SIGNATURES = {
     "kvq_decode_combine": (_int, [ctypes.POINTER(kvq_decode_params), _P, _P, _P, _P]),
     "kvq_decode": (_int, [ctypes.POINTER(kvq_cache), ctypes.POINTER(kvq_decode_params), _P, _P,
                           _P, _P, _P, _P]),
+    "kvq_decode_noalloc": (_int, [ctypes.POINTER(kvq_cache), ctypes.POINTER(kvq_decode_params),
+                                  _P, _P, _P]),
     "kvq_encode_e4m3": (_int, [_P, _P, _sz, _P]),
     "kvq_encode_e2m1": (_int, [_P, _P, _sz, _P]),
 }
@@ -175,6 +178,13 @@ def kvq_decode(cache: kvq_cache, params: kvq_decode_params, q, part_o, part_lse,
                out, stream=None) -> int:
     return lib().kvq_decode(_ref(cache), _ref(params), _addr(q), _addr(part_o), _addr(part_lse),
                             _addr(counters), _addr(out), _stream(stream))
+
+
+def kvq_decode_noalloc(cache: kvq_cache, params: kvq_decode_params, q, out, stream=None) -> int:
+    """kvq_decode with the library's own static scratch buffer: for callers
+    that cannot allocate device memory for split partials (see kvq.h)."""
+    return lib().kvq_decode_noalloc(_ref(cache), _ref(params), _addr(q), _addr(out),
+                                    _stream(stream))
 
 
 def kvq_encode_e4m3(x, out, n: int, stream=None) -> int:
