@@ -427,7 +427,8 @@ def sweep(device, args):
     res = []
     plans = [("gqa_fp8", synth.gqa_fp8, [1024, 8192, 32768], [1, 2, 4, 8, 0]),
              ("nvfp4", synth.nvfp4, [2048, 8192, 32768], [1, 2, 4, 8, 0]),
-             ("paged_fp8_probs", lambda L: synth.paged_fp8_probs(), [0], [1, 2, 0])]
+             ("paged_fp8_probs", lambda L: synth.paged_fp8_probs(), [0], [1, 2, 0]),
+             ("mla_nvfp4", lambda L: synth.mla_nvfp4(), [0], [1, 2, 4, 8, 0])]
     for name, mk, lens, splits in plans:
         for L in lens:
             w = mk(L) if L else mk(None)
