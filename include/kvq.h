@@ -168,11 +168,12 @@ kvq_status kvq_quantize_append(const kvq_cache* c, const void* k_new, const void
 /*
  * Split-count heuristic (host only, deterministic).  base = batch *
  * num_kv_heads (MLA: batch) CTAs per split; the partial kernel keeps three
- * CTAs resident per SM, so s = floor(3 * num_sms / base) fills one wave.  s
- * is then lowered so that every chunk keeps at least 128 tokens and clamped
- * to [1, 64].  num_sms is the device's multiprocessor count
- * (cudaDevAttrMultiProcessorCount).  q_per_kv and fmt are accepted for
- * tuning and currently do not change the result.
+ * CTAs resident per SM (two when q_per_kv > 8, e.g. MLA's 16 heads), so
+ * s = floor(ctas_per_sm * num_sms / base) fills one wave.  s is then lowered
+ * so that every chunk keeps at least 128 tokens and clamped to [1, 64].
+ * num_sms is the device's multiprocessor count
+ * (cudaDevAttrMultiProcessorCount).  fmt is accepted for tuning and
+ * currently does not change the result.
  */
 kvq_status kvq_auto_splits(int num_sms, int batch, int num_kv_heads, int q_per_kv,
                            int max_kv_len, int fmt, int* out_s /* host */);

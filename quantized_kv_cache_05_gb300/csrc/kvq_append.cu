@@ -50,14 +50,16 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(const AppendArgs a) {
   const int h = (int)(row % a.Hkv);
   const size_t bt = row / a.Hkv;
   const int tt = (int)(bt % a.T), b = (int)(bt / a.T);
-  const long dst_row = cache_row(a, b, __ldg(a.start_pos + b) + tt, h);
-  if (dst_row < 0) return;
   const bool isv = blockIdx.y == 1;
   const uint16_t* src = isv ? a.v_new : a.k_new;
+  // the row is read while the block-table lookup is in flight
+  const uint4 x = *reinterpret_cast<const uint4*>(src + row * a.D + part * 8);
+  const long dst_row = cache_row(a, b, __ldg(a.start_pos + b) + tt, h);
+  if (dst_row < 0) return;
   uint8_t* dst = isv ? a.v_codes : a.k_codes;
   const float s = isv ? a.v_scale : a.k_scale;
   float f[8];
-  bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + row * a.D + part * 8), f);
+  bf16x8_to_f32(x, f);
   uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
                 (f32x2_to_e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
   uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s)) |
@@ -97,13 +99,16 @@ __global__ void __launch_bounds__(256) append_nvfp4_kernel(const AppendArgs a) {
   const int h = (int)(row % a.Hkv);
   const size_t bt = row / a.Hkv;
   const int tt = (int)(bt % a.T), b = (int)(bt / a.T);
-  const long dst_row = cache_row(a, b, __ldg(a.start_pos + b) + tt, h);
-  if (dst_row < 0) return;
   const bool isv = blockIdx.y == 1;
   const uint16_t* src = (isv ? a.v_new : a.k_new) + row * a.D + blk * 16;
+  // the block is read while the block-table lookup is in flight
+  const uint4 x0 = *reinterpret_cast<const uint4*>(src);
+  const uint4 x1 = *reinterpret_cast<const uint4*>(src + 8);
+  const long dst_row = cache_row(a, b, __ldg(a.start_pos + b) + tt, h);
+  if (dst_row < 0) return;
   float f[16];
-  bf16x8_to_f32(*reinterpret_cast<const uint4*>(src), f);
-  bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + 8), f + 8);
+  bf16x8_to_f32(x0, f);
+  bf16x8_to_f32(x1, f + 8);
   uint32_t w0, w1;
   uint8_t sc;
   nvfp4_block(f, isv ? a.v_scale : a.k_scale, w0, w1, sc);

@@ -190,15 +190,33 @@ __device__ __forceinline__ void store_out(void* out, int dtype, float out_scale,
 // Merge of the s split partials of `rows` consecutive query heads starting at
 // partial row `row0` (M = max lse, w_j = e^(lse_j - M), O = sum w_j o_j /
 // sum w_j; O = 0 when every split is empty), written to `out` in the
-// requested type.  One warp per head row computes the weights (warp
-// reductions); all threads then sum the partials with eight independent
-// loads in flight.  w: rows * kMaxFusedSplits floats of shared memory (s <=
-// kMaxFusedSplits), winv: rows floats.  The caller synchronizes before.
-__device__ __forceinline__ void merge_rows(const float* part_o, const float* part_lse,
-                                           size_t row0, int rows, int s, int Dv, float* w,
-                                           float* winv, void* out, int out_dtype,
-                                           float out_scale) {
+// requested type.  Each thread owns float4 columns (four consecutive value
+// dims of one row) and reads up to kMergeDepth splits of a column at once;
+// the loads of its first column are issued before the weights are known, so
+// that one memory round trip covers the lse and the partials.  One warp per
+// head row computes the weights (warp reductions).  w: rows *
+// kMaxFusedSplits floats of shared memory (s <= kMaxFusedSplits), winv: rows
+// floats.  The caller synchronizes before.
+constexpr int kMergeDepth = 32;
+
+__device__ __forceinline__ void merge_rows(const float* __restrict__ part_o,
+                                           const float* __restrict__ part_lse, size_t row0,
+                                           int rows, int s, int Dv, float* w, float* winv,
+                                           void* out, int out_dtype, float out_scale) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nq = Dv / 4;
+  const int items = rows * nq;
+  float4 v[kMergeDepth];
+  auto load = [&](int i, int j0) {
+    const float4* po =
+        reinterpret_cast<const float4*>(part_o + (row0 + i / nq) * (size_t)s * Dv) + i % nq;
+#pragma unroll
+    for (int k = 0; k < kMergeDepth; ++k)
+      v[k] = j0 + k < s ? __ldcg(po + (size_t)(j0 + k) * nq) : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  const int i0 = threadIdx.x;
+  if (i0 < items) load(i0, 0);
+
   for (int r = warp; r < rows; r += blockDim.x >> 5) {
     const float* lse = part_lse + (row0 + r) * s;
     float lv[kMaxFusedSplits / 32];
@@ -215,30 +233,23 @@ __device__ __forceinline__ void merge_rows(const float* part_o, const float* par
 #pragma unroll
     for (int k = 0; k < kMaxFusedSplits / 32; ++k) {
       const int j = lane + 32 * k;
-      const float v = (M == -INFINITY || lv[k] == -INFINITY) ? 0.f : expf(lv[k] - M);
-      if (j < s) w[r * kMaxFusedSplits + j] = v;
-      sum += v;
+      const float e = (M == -INFINITY || lv[k] == -INFINITY) ? 0.f : expf(lv[k] - M);
+      if (j < s) w[r * kMaxFusedSplits + j] = e;
+      sum += e;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (lane == 0) winv[r] = sum > 0.f ? 1.f / sum : (sum == 0.f ? 0.f : NAN);
   }
   __syncthreads();
-  // four consecutive value dims per thread (float4), sixteen splits in flight
-  const int nq = Dv / 4;
-  for (int i = threadIdx.x; i < rows * nq; i += blockDim.x) {
-    const int r = i / nq, d4 = i % nq;
-    const float4* po =
-        reinterpret_cast<const float4*>(part_o + (row0 + r) * (size_t)s * Dv) + d4;
+  for (int i = i0; i < items; i += blockDim.x) {
+    const int r = i / nq;
     const float* wr = w + r * kMaxFusedSplits;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j0 = 0; j0 < s; j0 += 16) {
-      float4 v[16];
+    for (int j0 = 0; j0 < s; j0 += kMergeDepth) {
+      if (i != i0 || j0 != 0) load(i, j0);
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        v[k] = j0 + k < s ? __ldcg(po + (size_t)(j0 + k) * nq) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
+      for (int k = 0; k < kMergeDepth; ++k) {
         const float wk = j0 + k < s ? wr[j0 + k] : 0.f;
         acc.x += wk * v[k].x;
         acc.y += wk * v[k].y;
@@ -247,7 +258,7 @@ __device__ __forceinline__ void merge_rows(const float* part_o, const float* par
       }
     }
     const float iv = winv[r];
-    const size_t o = (row0 + r) * Dv + 4 * d4;
+    const size_t o = (row0 + r) * Dv + 4 * (i % nq);
     store_out(out, out_dtype, out_scale, o + 0, acc.x * iv);
     store_out(out, out_dtype, out_scale, o + 1, acc.y * iv);
     store_out(out, out_dtype, out_scale, o + 2, acc.z * iv);
@@ -257,24 +268,29 @@ __device__ __forceinline__ void merge_rows(const float* part_o, const float* par
 
 // Fused combine: the last CTA of a (request, kv head) to finish merges the
 // s partials of its G query heads and writes the output; it then resets the
-// arrival counter for the next call.  wbuf: kMaxGroup * (kMaxFusedSplits + 1)
-// floats of shared memory.
+// arrival counter for the next call.  The arrival is one acq_rel atomic by
+// thread 0 after a CTA barrier: its release orders the CTA's partial stores
+// (made before the barrier) before the arrival, and in the last CTA its
+// acquire, extended to the CTA by the second barrier, makes every other
+// CTA's partials visible.  wbuf: kMaxGroup * (kMaxFusedSplits + 1) floats of
+// shared memory.
 __device__ __forceinline__ void fused_combine(const PartialArgs& a, int bh, size_t part_row,
                                               float* wbuf) {
   __shared__ int is_last;
-  __threadfence();      // this CTA's partials are visible before it arrives
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(a.counters + bh, 1u);
+    unsigned prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(prev)
+                 : "l"(a.counters + bh)
+                 : "memory");
     is_last = prev == (unsigned)(a.num_splits - 1);
     if (is_last) a.counters[bh] = 0u;
   }
   __syncthreads();
   if (!is_last) return;
-  __threadfence();      // ... and the other CTAs' partials before we read them
   merge_rows(a.part_o, a.part_lse, part_row, a.G, a.num_splits, a.Dv, wbuf,
              wbuf + kMaxGroup * kMaxFusedSplits, a.out, a.out_dtype, a.out_scale);
 }
-
 
 }  // namespace kvq

@@ -78,13 +78,23 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
   const uint32_t ring = (smem_u32(dyn_smem) + 1023u) & ~1023u;
   const uint32_t scores = ring + Gm::kRing;   // FP8-prob mode only
 
-  // inputs may come from the previous kernel in the stream (launched with
-  // programmatic serialization, this kernel can start before it ends)
+  const int cap = min(a.max_pages * a.ps, a.max_kv_len);
+  // Launched with programmatic serialization, this kernel can start before
+  // the previous kernel in the stream ends, and its inputs may come from that
+  // kernel.  Before the wait it only sets up its barriers.
+  if (threadIdx.x == 0) sm.abort_flag = 0;
+  if (lane == 0) {
+    for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&sm.full[warp][i]), 1);
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
   griddep_wait();
 
   // chunk of this split
   int L = a.seq_lens[b];
-  const int cap = min(a.max_pages * a.ps, a.max_kv_len);
   if (L > cap || L < 0) {
     if (threadIdx.x == 0) record_error(a.error_flag, 2);
     L = L < 0 ? 0 : cap;
@@ -109,11 +119,6 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
       pg = 0;
     }
     sm.pages[i] = pg;
-  }
-  if (threadIdx.x == 0) sm.abort_flag = 0;
-  if (lane == 0) {
-    for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&sm.full[warp][i]), 1);
-    fence_barrier_init();
   }
   __syncthreads();
   volatile int* abort_flag = &sm.abort_flag;
@@ -157,11 +162,8 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
   };
 
   int issued = 0;
-  if (lane == 0) {
-    prefetch_tmap(&tmK);
-    prefetch_tmap(&tmV);
+  if (lane == 0)
     for (; issued < min(total, kStages); ++issued) issue(issued);
-  }
 
   const int hq0 = h * a.G;
   // Q^T fragments (B operand of S^T = K Q^T: k = head dims, n = query heads
@@ -419,25 +421,20 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
         sm.l[warp][2 * t + e + 8 * hh] = l[hh][e];
       }
   }
-  // O tiles go to the (drained) ring: obuf[warp][head][swizzled d], heads < G
-  __syncthreads();
-  float* obuf = reinterpret_cast<float*>(dyn_smem + (ring - smem_u32(dyn_smem)));
-  const bool bad = *abort_flag != 0;
-  if (!bad) {
-#pragma unroll
-    for (int i = 0; i < MT; ++i)
-#pragma unroll
-      for (int hh = 0; hh < NH; ++hh)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int head = 2 * t + (e & 1) + 8 * hh;
-          const int d = (D / 8) * g + 2 * i + (e >> 1);
-          if (head < a.G) obuf[(warp * a.G + head) * D + obuf_swz<D>(head, d)] = o[i][hh][e];
-        }
-  }
-  __syncthreads();
+  __syncthreads();   // every warp's ring is drained; m and l are in shared memory
 
-  // ---------------------------------------------------------------- merge
+  // O fragments -> the ring in fragment order, one 16-byte store per m-tile:
+  // ofrag[warp][i][hh][lane] = (d0, 2t) (d0, 2t+1) (d0+1, 2t) (d0+1, 2t+1)
+  // with d0 = (D/8) g + 2i, heads 2t + 8hh.  Meanwhile the first G threads
+  // compute the warps' merge factors and the chunk's lse.
+  float4* ofrag = reinterpret_cast<float4*>(dyn_smem + (ring - smem_u32(dyn_smem)));
+  const bool bad = *abort_flag != 0;
+#pragma unroll
+  for (int i = 0; i < MT; ++i)
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh)
+      ofrag[((warp * MT + i) * NH + hh) * 32 + lane] =
+          make_float4(o[i][hh][0], o[i][hh][1], o[i][hh][2], o[i][hh][3]);
   const size_t part_row = ((size_t)b * a.Hq + (size_t)h * a.G);   // first query head
   if (threadIdx.x < a.G) {
     const int row = threadIdx.x;
@@ -455,19 +452,33 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
     a.part_lse[(part_row + row) * a.num_splits + split] = lse;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < a.G * D; i += blockDim.x) {
-    const int row = i / D, d = i % D;
-    float acc = 0.f;
-    if (!bad) {
+
+  // ---------------------------------------------------------------- merge
+  // item (i, hh, lane'): heads h0 = 2t' + 8hh and h0 + 1, dims d0 and d0 + 1
+  for (int it = threadIdx.x; it < MT * NH * 32; it += kDecodeThreads) {
+    const int ln = it & 31, hh = (it >> 5) % NH, i = (it >> 5) / NH;
+    const int h0 = 2 * (ln & 3) + 8 * hh;
+    if (h0 >= a.G) continue;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int w = 0; w < kDecodeWarps; ++w)
-        acc += sm.fac[w][row] * obuf[(w * a.G + row) * D + obuf_swz<D>(row, d)];
-    } else {
-      acc = NAN;
+    for (int w = 0; w < kDecodeWarps; ++w) {
+      const float4 v = ofrag[((w * MT + i) * NH + hh) * 32 + ln];
+      const float f0 = sm.fac[w][h0], f1 = sm.fac[w][h0 + 1];
+      acc.x += f0 * v.x;
+      acc.y += f1 * v.y;
+      acc.z += f0 * v.z;
+      acc.w += f1 * v.w;
     }
-    a.part_o[((part_row + row) * a.num_splits + split) * D + d] = acc;
+    if (bad) acc = make_float4(NAN, NAN, NAN, NAN);
+    const int d0 = (D / 8) * (ln >> 2) + 2 * i;
+    float* r0 = a.part_o + ((part_row + h0) * a.num_splits + split) * D + d0;
+    *reinterpret_cast<float2*>(r0) = make_float2(acc.x, acc.z);
+    if (h0 + 1 < a.G) *reinterpret_cast<float2*>(r0 + (size_t)a.num_splits * D) =
+        make_float2(acc.y, acc.w);
   }
-  if (a.counters) fused_combine(a, bh, part_row, obuf + kDecodeWarps * kMaxGroup * D);
+  if (a.counters)
+    fused_combine(a, bh, part_row,
+                  reinterpret_cast<float*>(ofrag + kDecodeWarps * MT * NH * 32));
 }
 
 // ---------------------------------------------------------------------------
@@ -488,10 +499,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
 template <int FMT, int D, bool PROBQ, int NH>
 cudaError_t launch_partial_t(const TensorMaps& m, const PartialArgs& a, cudaStream_t st) {
   using Gm = Geom<FMT, D>;
-  static_assert((size_t)kDecodeWarps * kMaxGroup * D * 4 +
+  static_assert((size_t)kDecodeWarps * Gm::kMT * NH * 32 * 16 +
                         (size_t)(kMaxGroup * kMaxFusedSplits + kMaxGroup) * 4 <=
                     (size_t)Gm::kRing,
-                "the merge buffer and the combine weights must fit in the ring");
+                "the O fragments and the combine weights must fit in the ring");
   const size_t smem = 1024 + (size_t)Gm::kRing + (PROBQ ? (size_t)a.score_floats * 4 : 0);
   auto kern = partial_kernel<FMT, D, PROBQ, NH>;
   cudaError_t e =

@@ -85,10 +85,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   float* sx = reinterpret_cast<float*>(dyn_smem + (ring - smem_u32(dyn_smem)) + kMlaRing);
   float* wbuf = sx + kMlaSxFloats;
 
+  const int cap = min(a.max_pages * a.ps, a.max_kv_len);
+  // only barrier setup before the grid-dependency wait
+  if (threadIdx.x == 0) sm.abort_flag = 0;
+  if (lane == 0) {
+    for (int i = 0; i < kMlaStages; ++i) mbar_init(smem_u32(&sm.full[warp][i]), 1);
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&tmKv);
+    prefetch_tmap(&tmPe);
+  }
   griddep_wait();
 
   int L = a.seq_lens[b];
-  const int cap = min(a.max_pages * a.ps, a.max_kv_len);
   if (L > cap || L < 0) {
     if (threadIdx.x == 0) record_error(a.error_flag, 2);
     L = L < 0 ? 0 : cap;
@@ -109,11 +119,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
       pg = 0;
     }
     sm.pages[i] = pg;
-  }
-  if (threadIdx.x == 0) sm.abort_flag = 0;
-  if (lane == 0) {
-    for (int i = 0; i < kMlaStages; ++i) mbar_init(smem_u32(&sm.full[warp][i]), 1);
-    fence_barrier_init();
   }
   __syncthreads();
   volatile int* abort_flag = &sm.abort_flag;
@@ -142,11 +147,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     tma_load_3d(sbase + kMlaRopeOff, &tmPe, 0, warp, (int)row, full);
   };
   int issued = 0;
-  if (lane == 0) {
-    prefetch_tmap(&tmKv);
-    prefetch_tmap(&tmPe);
+  if (lane == 0)
     for (; issued < min(nboxes, kMlaStages); ++issued) issue(issued);
-  }
 
   // Q^T fragments: latent dims 128 w + 32 t + 4 j + {0..3} (permuted like
   // the K fragments) and rope dims 512 + 16 w + 4 t + {0..3} (bf16 as is)

@@ -71,10 +71,11 @@ def test_auto_splits():
     assert f(152, 1, 8, 4, 2048, 2) == (0, 16)
     # large batch: one split
     assert f(152, 64, 16, 1, 8192, 1) == (0, 1)
-    # MLA: base = batch = 32 -> floor(456 / 32) = 14
-    assert f(152, 32, 1, 16, 4096, 2) == (0, 14)
+    # MLA (16 heads on one kv head: two CTAs per SM): floor(304 / 32) = 9
+    assert f(152, 32, 1, 16, 4096, 2) == (0, 9)
+    assert f(152, 2, 1, 12, 32768, 1) == (0, 64)
     # clamp at 64
-    assert f(152, 1, 1, 16, 1 << 20, 2) == (0, 64)
+    assert f(152, 1, 1, 4, 1 << 20, 2) == (0, 64)
     assert f(0, 1, 1, 1, 10, 1)[0] == kvq.KVQ_ERR_INVALID
     assert f(152, 0, 1, 1, 10, 1)[0] == kvq.KVQ_ERR_INVALID
 
