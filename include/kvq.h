@@ -120,6 +120,20 @@ typedef struct kvq_decode_params {
   int32_t out_dtype;         /* KVQ_OUT_* (used by combine) */
   float out_scale;           /* KVQ_OUT_E4M3: output scale, finite > 0 */
   int32_t* error_flag;       /* (device, optional) KVQ_DEVERR_* bits OR-ed in */
+  /*
+   * Overlap with the append of this step (>= 0).  0: the decode waits for
+   * the preceding kernel in the stream to finish before it reads any input
+   * (always correct).  n > 0 declares that the work issued immediately
+   * before on the same stream is one kvq_quantize_append call that wrote
+   * only positions seq_lens[b] - n .. seq_lens[b] - 1 of each request, and
+   * that q, seq_lens, the block table and every other cache position were
+   * complete when that call was made (kvq_quantize_append starts after all
+   * earlier work in the stream).  The decode then streams every other part
+   * of the cache while the append runs and waits for it only before the
+   * boxes that hold those positions.  Not part of the papers' method: a
+   * scheduling contract between two calls of this library.
+   */
+  int32_t fresh_tokens;
 } kvq_decode_params;
 
 /* Human-readable name of a status code (static string). */

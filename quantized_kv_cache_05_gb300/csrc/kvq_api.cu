@@ -104,6 +104,7 @@ kvq_status check_params(const kvq_decode_params* p) {
   if (!std::isfinite(p->prob_scale) || p->prob_scale < 0.f) return KVQ_ERR_INVALID;
   if (p->out_dtype < KVQ_OUT_F32 || p->out_dtype > KVQ_OUT_E4M3) return KVQ_ERR_INVALID;
   if (p->out_dtype == KVQ_OUT_E4M3 && !finite_pos(p->out_scale)) return KVQ_ERR_INVALID;
+  if (p->fresh_tokens < 0) return KVQ_ERR_INVALID;
   return KVQ_OK;
 }
 
@@ -274,6 +275,7 @@ kvq_status decode_impl(const kvq_cache* c, const kvq_decode_params* p, const voi
   a.score_floats = (int)score_floats;
   a.qk_scale_log2 = p->sm_scale * c->k_scale * 1.4426950408889634f;
   a.prob_scale = p->prob_scale;
+  a.fresh = p->fresh_tokens;
   a.counters = counters;
   a.out = out;
   a.out_dtype = p->out_dtype;

@@ -81,7 +81,9 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
   const int cap = min(a.max_pages * a.ps, a.max_kv_len);
   // Launched with programmatic serialization, this kernel can start before
   // the previous kernel in the stream ends, and its inputs may come from that
-  // kernel.  Before the wait it only sets up its barriers.
+  // kernel.  Before the wait it only sets up its barriers -- unless the
+  // caller declared that kernel to be the append of the last a.fresh
+  // positions: then only the loads of boxes holding those positions wait.
   if (threadIdx.x == 0) sm.abort_flag = 0;
   if (lane == 0) {
     for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&sm.full[warp][i]), 1);
@@ -91,7 +93,7 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
   }
-  griddep_wait();
+  if (a.fresh == 0) griddep_wait();
 
   // chunk of this split
   int L = a.seq_lens[b];
@@ -104,6 +106,9 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
   const int cstart = (int)min((long)split * c, (long)L);
   const int cend = (int)min((long)cstart + c, (long)L);
   const int nboxes = (cend - cstart + kBoxTokens - 1) / kBoxTokens;
+  // first box of the chunk that holds an appended position (overlap mode)
+  const int fresh_box = a.fresh == 0 ? 0 : (max(L - a.fresh, cstart) - cstart) / kBoxTokens;
+  bool dep_done = a.fresh == 0;   // this thread has waited for the preceding kernel
   // this warp's boxes: warp, warp + 4, ...
   const int nw = nboxes > warp ? (nboxes - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
   const int total = kSweeps * nw;
@@ -143,6 +148,10 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
       }
     }
     const long row = ((long)page * a.Hkv + h) * a.ps + (tok % a.ps);
+    if (!dep_done && box >= fresh_box) {
+      griddep_wait();
+      dep_done = true;
+    }
     const int st = j % kStages;
     const uint32_t full = smem_u32(&sm.full[warp][st]);
     const uint32_t sbase = ring + (warp * kStages + st) * Gm::kStage;
@@ -436,6 +445,8 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
       ofrag[((warp * MT + i) * NH + hh) * 32 + lane] =
           make_float4(o[i][hh][0], o[i][hh][1], o[i][hh][2], o[i][hh][3]);
   const size_t part_row = ((size_t)b * a.Hq + (size_t)h * a.G);   // first query head
+  // the grid ends after the preceding kernel in every mode
+  if (!dep_done && threadIdx.x == 0) griddep_wait();
   if (threadIdx.x < a.G) {
     const int row = threadIdx.x;
     float M = -INFINITY;

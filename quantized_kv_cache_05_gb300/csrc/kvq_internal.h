@@ -56,6 +56,7 @@ struct PartialArgs {
   float pe_scale_log2;        // MLA rope part: sm_scale * log2(e)
   float out_mult;             // v_scale (times prob_scale with FP8 probabilities)
   float prob_scale;           // > 0: FP8 probabilities
+  int fresh;                  // > 0: only the last `fresh` positions wait for the append
   // fused combine (kvq_decode): arrival counters [B * Hkv] and the output
   uint32_t* counters;         // null: partials only
   void* out;

@@ -96,7 +96,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     prefetch_tmap(&tmKv);
     prefetch_tmap(&tmPe);
   }
-  griddep_wait();
+  // overlap mode (a.fresh > 0): only the loads of boxes that hold the last
+  // a.fresh positions wait for the preceding append
+  if (a.fresh == 0) griddep_wait();
 
   int L = a.seq_lens[b];
   if (L > cap || L < 0) {
@@ -108,6 +110,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   const int cstart = (int)min((long)split * c, (long)L);
   const int cend = (int)min((long)cstart + c, (long)L);
   const int nboxes = (cend - cstart + kBoxTokens - 1) / kBoxTokens;   // all warps, all boxes
+  const int fresh_box = a.fresh == 0 ? 0 : (max(L - a.fresh, cstart) - cstart) / kBoxTokens;
+  bool dep_done = a.fresh == 0;
 
   const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
   const int p0 = cstart / a.ps;
@@ -138,6 +142,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
       }
     }
     const long row = (long)page * a.ps + (tok % a.ps);
+    if (!dep_done && j >= fresh_box) {
+      griddep_wait();
+      dep_done = true;
+    }
     const int st = j % kMlaStages;
     const uint32_t full = smem_u32(&sm.full[warp][st]);
     const uint32_t sbase = ring + (warp * kMlaStages + st) * kMlaStage;
@@ -307,6 +315,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
       l[hh][e] = v;
     }
   __syncthreads();
+  if (!dep_done && threadIdx.x == 0) griddep_wait();   // the grid ends after the append
   const bool bad = *abort_flag != 0;
   // normalized O of this warp's dims -> shared memory obuf[head][512] (the ring
   // is drained), then coalesced stores of the partials

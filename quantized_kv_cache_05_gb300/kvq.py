@@ -46,6 +46,7 @@ class kvq_decode_params(ctypes.Structure):
         ("batch", _i32), ("num_q_heads", _i32), ("qk_dim", _i32), ("v_dim", _i32),
         ("num_splits", _i32), ("seq_lens", _P), ("max_kv_len", _i32), ("sm_scale", _f),
         ("prob_scale", _f), ("out_dtype", _i32), ("out_scale", _f), ("error_flag", _P),
+        ("fresh_tokens", _i32),
     ]
 
 

@@ -90,6 +90,9 @@ class DecodeConfig:
     prob_scale: float = 0.0
     out: str = "f32"
     out_scale: float = 1.0
+    # > 0: the call right before on the stream is the append of the last
+    # fresh_tokens positions, and the decode overlaps with it (kvq_decode_params)
+    fresh_tokens: int = 0
 
     def params(self, seq_lens: torch.Tensor, error_flag: Optional[torch.Tensor] = None
                ) -> kvq.kvq_decode_params:
@@ -101,6 +104,7 @@ class DecodeConfig:
         p.sm_scale, p.prob_scale = self.sm_scale, self.prob_scale
         p.out_dtype, p.out_scale = OUT[self.out], self.out_scale
         p.error_flag = error_flag.data_ptr() if error_flag is not None else None
+        p.fresh_tokens = self.fresh_tokens
         return p
 
 

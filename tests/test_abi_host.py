@@ -120,6 +120,7 @@ def good_params():
     lambda c, p: setattr(p, "max_kv_len", 65),          # beyond 4 pages x 16
     lambda c, p: setattr(p, "seq_lens", None),
     lambda c, p: setattr(p, "qk_dim", 64),
+    lambda c, p: setattr(p, "fresh_tokens", -1),
     lambda c, p: (setattr(c, "fmt", 2)),                 # NVFP4 without block scales
 ], ids=lambda f: "case")
 def test_decode_partial_rejects_without_launch(L, mutate):
