@@ -1,6 +1,7 @@
 // The extern "C" entry points of include/kvq.h: argument validation (before
 // any launch), TMA descriptor setup and kernel dispatch.  Host code only.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -196,15 +197,18 @@ kvq_status kvq_quantize_append(const kvq_cache* c, const void* k_new, const void
 
 kvq_status kvq_auto_splits(int num_sms, int batch, int num_kv_heads, int q_per_kv,
                            int max_kv_len, int fmt, int* out_s) {
-  (void)fmt;
   if (!out_s || num_sms < 1 || batch < 1 || num_kv_heads < 1 || max_kv_len < 0)
     return KVQ_ERR_INVALID;
-  // One wave of the partial kernel: three resident CTAs per SM, two for the
-  // kernels with more than eight query heads per kv head (MLA's 16).
-  constexpr long long kMinChunk = 128, kMaxSplits = 64;
+  // One wave of the partial kernel (three resident CTAs per SM, two with
+  // more than eight query heads per kv head, e.g. MLA's 16), and chunks of
+  // at most kTargetChunk tokens, so that long or ragged requests are cut
+  // into pieces that balance across the waves.
+  (void)fmt;
+  constexpr long long kMinChunk = 128, kMaxSplits = 64, kTargetChunk = 2048;
   const long long ctas_per_sm = q_per_kv > 8 ? 2 : 3;
   const long long base = (long long)batch * num_kv_heads;
   long long s = ctas_per_sm * num_sms / base;
+  s = std::max(s, ((long long)max_kv_len + kTargetChunk - 1) / kTargetChunk);
   const long long by_len = max_kv_len / kMinChunk;
   if (s > by_len) s = by_len;
   if (s < 1) s = 1;

@@ -23,6 +23,9 @@ struct Geom {
   // every stage starts on the 1024-byte swizzle period
   static constexpr int kStage = (2 * (kBoxK + kBoxS) + 1023) / 1024 * 1024;
   static constexpr int kRing = kDecodeWarps * kStages * kStage;
+  // FP8-probability mode streams K and V in separate sweeps: a stage holds
+  // one box of one tensor, [codes][scales]
+  static constexpr int kStage1 = (kBoxK + kBoxS + 1023) / 1024 * 1024;
   static constexpr int kKSteps = D / 16;   // QK k-steps over head_dim
   static constexpr int kMT = D / 16;       // PV m-tiles over v_dim
   // physical 16-byte chunk of logical chunk `ch` in row `row` of a box
@@ -191,14 +194,13 @@ __device__ __forceinline__ void store_out(void* out, int dtype, float out_scale,
 // partial row `row0` (M = max lse, w_j = e^(lse_j - M), O = sum w_j o_j /
 // sum w_j; O = 0 when every split is empty), written to `out` in the
 // requested type.  Each thread owns float4 columns (four consecutive value
-// dims of one row) and reads up to kMergeDepth splits of a column at once;
+// dims of one row) and reads up to DEPTH splits of a column at once;
 // the loads of its first column are issued before the weights are known, so
 // that one memory round trip covers the lse and the partials.  One warp per
 // head row computes the weights (warp reductions).  w: rows *
 // kMaxFusedSplits floats of shared memory (s <= kMaxFusedSplits), winv: rows
 // floats.  The caller synchronizes before.
-constexpr int kMergeDepth = 32;
-
+template <int DEPTH = 32>
 __device__ __forceinline__ void merge_rows(const float* __restrict__ part_o,
                                            const float* __restrict__ part_lse, size_t row0,
                                            int rows, int s, int Dv, float* w, float* winv,
@@ -206,12 +208,12 @@ __device__ __forceinline__ void merge_rows(const float* __restrict__ part_o,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq = Dv / 4;
   const int items = rows * nq;
-  float4 v[kMergeDepth];
+  float4 v[DEPTH];
   auto load = [&](int i, int j0) {
     const float4* po =
         reinterpret_cast<const float4*>(part_o + (row0 + i / nq) * (size_t)s * Dv) + i % nq;
 #pragma unroll
-    for (int k = 0; k < kMergeDepth; ++k)
+    for (int k = 0; k < DEPTH; ++k)
       v[k] = j0 + k < s ? __ldcg(po + (size_t)(j0 + k) * nq) : make_float4(0.f, 0.f, 0.f, 0.f);
   };
   const int i0 = threadIdx.x;
@@ -246,10 +248,10 @@ __device__ __forceinline__ void merge_rows(const float* __restrict__ part_o,
     const int r = i / nq;
     const float* wr = w + r * kMaxFusedSplits;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j0 = 0; j0 < s; j0 += kMergeDepth) {
+    for (int j0 = 0; j0 < s; j0 += DEPTH) {
       if (i != i0 || j0 != 0) load(i, j0);
 #pragma unroll
-      for (int k = 0; k < kMergeDepth; ++k) {
+      for (int k = 0; k < DEPTH; ++k) {
         const float wk = j0 + k < s ? wr[j0 + k] : 0.f;
         acc.x += wk * v[k].x;
         acc.y += wk * v[k].y;
@@ -273,7 +275,8 @@ __device__ __forceinline__ void merge_rows(const float* __restrict__ part_o,
 // (made before the barrier) before the arrival, and in the last CTA its
 // acquire, extended to the CTA by the second barrier, makes every other
 // CTA's partials visible.  wbuf: kMaxGroup * (kMaxFusedSplits + 1) floats of
-// shared memory.
+// shared memory.  DEPTH: merge_rows' load depth (register budget).
+template <int DEPTH = 32>
 __device__ __forceinline__ void fused_combine(const PartialArgs& a, int bh, size_t part_row,
                                               float* wbuf) {
   __shared__ int is_last;
@@ -289,7 +292,7 @@ __device__ __forceinline__ void fused_combine(const PartialArgs& a, int bh, size
   }
   __syncthreads();
   if (!is_last) return;
-  merge_rows(a.part_o, a.part_lse, part_row, a.G, a.num_splits, a.Dv, wbuf,
+  merge_rows<DEPTH>(a.part_o, a.part_lse, part_row, a.G, a.num_splits, a.Dv, wbuf,
              wbuf + kMaxGroup * kMaxFusedSplits, a.out, a.out_dtype, a.out_scale);
 }
 

@@ -55,9 +55,30 @@ struct Smem {
   float fac[kDecodeWarps][kMaxGroup];
 };
 
+// Shared-memory ring of the partial kernel: the TMA stages, reused after the
+// loop for the warps' O fragments and the fused combine's weights.
+template <int FMT, int D, bool PROBQ, int NH>
+struct Ring {
+  using Gm = Geom<FMT, D>;
+  static constexpr int kStageBytes = PROBQ ? Gm::kStage1 : Gm::kStage;
+  static constexpr int kEpilogue = kDecodeWarps * Gm::kMT * NH * 32 * 16 +
+                                   (kMaxGroup * kMaxFusedSplits + kMaxGroup) * 4;
+  static constexpr int kStream = kDecodeWarps * kStages * kStageBytes;
+  static constexpr int kBytes =
+      kStream > kEpilogue ? kStream : (kEpilogue + 1023) / 1024 * 1024;
+};
+
+// Resident CTAs per SM the kernel is compiled for: four for the half-size
+// ring of the FP8-probability mode with up to eight query heads per kv head,
+// three otherwise, two with sixteen heads (twice the accumulators).
+template <int FMT, bool PROBQ, int NH>
+constexpr int ctas_per_sm() {
+  return NH == 2 ? 2 : PROBQ ? 4 : 3;
+}
+
 // NH = number of 8-head groups (1: up to 8 query heads per kv head, 2: up to 16)
 template <int FMT, int D, bool PROBQ, int NH>
-__global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
+__global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, PROBQ, NH>())
     partial_kernel(const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PartialArgs a) {
   using Gm = Geom<FMT, D>;
@@ -76,7 +97,8 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
 
   // ring base, aligned for the 128-byte swizzle pattern
   const uint32_t ring = (smem_u32(dyn_smem) + 1023u) & ~1023u;
-  const uint32_t scores = ring + Gm::kRing;   // FP8-prob mode only
+  using Rg = Ring<FMT, D, PROBQ, NH>;
+  const uint32_t scores = ring + Rg::kBytes;   // FP8-prob mode only
 
   const int cap = min(a.max_pages * a.ps, a.max_kv_len);
   // Launched with programmatic serialization, this kernel can start before
@@ -154,19 +176,22 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
     }
     const int st = j % kStages;
     const uint32_t full = smem_u32(&sm.full[warp][st]);
-    const uint32_t sbase = ring + (warp * kStages + st) * Gm::kStage;
+    const uint32_t sbase = ring + (warp * kStages + st) * Rg::kStageBytes;
     const uint32_t bytes = (loadK ? Gm::kBoxK + Gm::kBoxS : 0) + (loadV ? Gm::kBoxK + Gm::kBoxS : 0);
     mbar_arrive_expect_tx(full, bytes);
-    if (loadK) {
+    if constexpr (PROBQ) {   // one tensor per stage: [codes][scales]
+      tma_load_2d(sbase, loadK ? &tmK : &tmV, 0, (int)row, full);
+      if constexpr (FMT == kFmtNvfp4)
+        bulk_load(sbase + Gm::kBoxK, (loadK ? a.k_bscale : a.v_bscale) + row * Gm::kSRow,
+                  Gm::kBoxS, full);
+    } else {                 // [K codes][V codes][K scales][V scales]
       tma_load_2d(sbase, &tmK, 0, (int)row, full);
-      if constexpr (FMT == kFmtNvfp4)
-        bulk_load(sbase + 2 * Gm::kBoxK, a.k_bscale + row * Gm::kSRow, Gm::kBoxS, full);
-    }
-    if (loadV) {
       tma_load_2d(sbase + Gm::kBoxK, &tmV, 0, (int)row, full);
-      if constexpr (FMT == kFmtNvfp4)
+      if constexpr (FMT == kFmtNvfp4) {
+        bulk_load(sbase + 2 * Gm::kBoxK, a.k_bscale + row * Gm::kSRow, Gm::kBoxS, full);
         bulk_load(sbase + 2 * Gm::kBoxK + Gm::kBoxS, a.v_bscale + row * Gm::kSRow, Gm::kBoxS,
                   full);
+      }
     }
   };
 
@@ -220,11 +245,11 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
       __syncwarp();   // the other lanes read the box after lane 0's acquire
       const int tbase = cstart + (warp + kDecodeWarps * jj) * kBoxTokens;
       const int nvalid = min(kBoxTokens, cend - tbase);
-      const uint32_t sbase = ring + (warp * kStages + st) * Gm::kStage;
+      const uint32_t sbase = ring + (warp * kStages + st) * Rg::kStageBytes;
       const uint32_t boxK = sbase;
-      const uint32_t boxV = sbase + Gm::kBoxK;
-      const uint32_t boxKs = sbase + 2 * Gm::kBoxK;
-      const uint32_t boxVs = boxKs + Gm::kBoxS;
+      const uint32_t boxV = PROBQ ? sbase : sbase + Gm::kBoxK;
+      const uint32_t boxKs = PROBQ ? sbase + Gm::kBoxK : sbase + 2 * Gm::kBoxK;
+      const uint32_t boxVs = PROBQ ? boxKs : boxKs + Gm::kBoxS;
       const int tok_in_chunk = tbase - cstart;
 
       // x[hh][e]: scaled score of token g + 8 (e >> 1), head 2t + (e & 1) + 8 hh
@@ -488,7 +513,7 @@ __global__ void __launch_bounds__(kDecodeThreads, NH == 1 ? 3 : 2)
         make_float2(acc.y, acc.w);
   }
   if (a.counters)
-    fused_combine(a, bh, part_row,
+    fused_combine<ctas_per_sm<FMT, PROBQ, NH>() == 4 ? 16 : 32>(a, bh, part_row,
                   reinterpret_cast<float*>(ofrag + kDecodeWarps * MT * NH * 32));
 }
 
@@ -509,12 +534,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
 
 template <int FMT, int D, bool PROBQ, int NH>
 cudaError_t launch_partial_t(const TensorMaps& m, const PartialArgs& a, cudaStream_t st) {
-  using Gm = Geom<FMT, D>;
-  static_assert((size_t)kDecodeWarps * Gm::kMT * NH * 32 * 16 +
-                        (size_t)(kMaxGroup * kMaxFusedSplits + kMaxGroup) * 4 <=
-                    (size_t)Gm::kRing,
-                "the O fragments and the combine weights must fit in the ring");
-  const size_t smem = 1024 + (size_t)Gm::kRing + (PROBQ ? (size_t)a.score_floats * 4 : 0);
+  using Rg = Ring<FMT, D, PROBQ, NH>;
+  static_assert(Rg::kBytes >= Rg::kEpilogue && Rg::kBytes >= Rg::kStream, "ring too small");
+  const size_t smem = 1024 + (size_t)Rg::kBytes + (PROBQ ? (size_t)a.score_floats * 4 : 0);
   auto kern = partial_kernel<FMT, D, PROBQ, NH>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -69,11 +69,15 @@ def test_auto_splits():
     # batch 1 x 8 kv heads: floor(456 / 8) = 57
     assert f(152, 1, 8, 4, 32768, 2) == (0, 57)
     assert f(152, 1, 8, 4, 2048, 2) == (0, 16)
-    # large batch: one split
-    assert f(152, 64, 16, 1, 8192, 1) == (0, 1)
+    # large batch: chunks of at most 2048 tokens (ceil(8192 / 2048) = 4)
+    assert f(152, 64, 16, 1, 8192, 1) == (0, 4)
+    assert f(152, 64, 16, 1, 2048, 1) == (0, 1)
+    assert f(152, 64, 16, 1, 2049, 1) == (0, 2)
+    assert f(152, 4, 8, 4, 200000, 1) == (0, 64)
     # MLA (16 heads on one kv head: two CTAs per SM): floor(304 / 32) = 9
     assert f(152, 32, 1, 16, 4096, 2) == (0, 9)
     assert f(152, 2, 1, 12, 32768, 1) == (0, 64)
+    assert f(152, 128, 1, 16, 4096, 2) == (0, 2)
     # clamp at 64
     assert f(152, 1, 1, 4, 1 << 20, 2) == (0, 64)
     assert f(0, 1, 1, 1, 10, 1)[0] == kvq.KVQ_ERR_INVALID
