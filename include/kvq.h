@@ -182,13 +182,13 @@ kvq_status kvq_quantize_append(const kvq_cache* c, const void* k_new, const void
 /*
  * Split-count heuristic (host only, deterministic).  base = batch *
  * num_kv_heads (MLA: batch) CTAs per split; the partial kernel keeps
- * ctas_per_sm CTAs resident per SM (3, or 2 when q_per_kv > 8, e.g. MLA's
- * 16 heads), so floor(ctas_per_sm * num_sms / base) splits fill one wave;
+ * ctas_per_sm CTAs resident per SM (3; 2 when q_per_kv > 8; 1 for the MLA
+ * shape: KVQ_NVFP4, num_kv_heads 1, q_per_kv 16), so
+ * floor(ctas_per_sm * num_sms / base) splits fill one wave;
  * s is at least ceil(max_kv_len / 2048), so that long or ragged requests
  * are cut into chunks that balance across waves.  s is then lowered so that
  * every chunk keeps at least 128 tokens and clamped to [1, 64].  num_sms is
- * the device's multiprocessor count (cudaDevAttrMultiProcessorCount).  fmt
- * is accepted for tuning and does not change the result.
+ * the device's multiprocessor count (cudaDevAttrMultiProcessorCount).
  */
 kvq_status kvq_auto_splits(int num_sms, int batch, int num_kv_heads, int q_per_kv,
                            int max_kv_len, int fmt, int* out_s /* host */);

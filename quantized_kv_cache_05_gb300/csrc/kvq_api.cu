@@ -53,14 +53,14 @@ bool make_row_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t
 }
 
 // 3-D byte view [rows][n_slices][slice_bytes] of a row-major tensor whose rows
-// are n_slices * slice_bytes wide; boxes of one slice x 16 rows.
+// are n_slices * slice_bytes wide; boxes of one slice x box_rows rows.
 bool make_slice_map(CUtensorMap* m, const void* base, uint64_t slice_bytes, uint64_t n_slices,
-                    uint64_t rows, CUtensorMapSwizzle sw) {
+                    uint64_t rows, CUtensorMapSwizzle sw, uint32_t box_rows = kBoxTokens) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {slice_bytes, n_slices, rows};
   cuuint64_t strides[2] = {slice_bytes, slice_bytes * n_slices};
-  cuuint32_t box[3] = {(cuuint32_t)slice_bytes, 1, (cuuint32_t)kBoxTokens};
+  cuuint32_t box[3] = {(cuuint32_t)slice_bytes, 1, box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -200,12 +200,13 @@ kvq_status kvq_auto_splits(int num_sms, int batch, int num_kv_heads, int q_per_k
   if (!out_s || num_sms < 1 || batch < 1 || num_kv_heads < 1 || max_kv_len < 0)
     return KVQ_ERR_INVALID;
   // One wave of the partial kernel (three resident CTAs per SM, two with
-  // more than eight query heads per kv head, e.g. MLA's 16), and chunks of
-  // at most kTargetChunk tokens, so that long or ragged requests are cut
-  // into pieces that balance across the waves.
-  (void)fmt;
+  // more than eight query heads per kv head, one for the MLA kernel: NVFP4,
+  // one kv head, 16 query heads), and chunks of at most kTargetChunk tokens,
+  // so that long or ragged requests are cut into pieces that balance across
+  // the waves.
   constexpr long long kMinChunk = 128, kMaxSplits = 64, kTargetChunk = 2048;
-  const long long ctas_per_sm = q_per_kv > 8 ? 2 : 3;
+  const bool mla_shape = fmt == KVQ_NVFP4 && num_kv_heads == 1 && q_per_kv == 16;
+  const long long ctas_per_sm = mla_shape ? 1 : q_per_kv > 8 ? 2 : 3;
   const long long base = (long long)batch * num_kv_heads;
   long long s = ctas_per_sm * num_sms / base;
   s = std::max(s, ((long long)max_kv_len + kTargetChunk - 1) / kTargetChunk);
@@ -291,13 +292,17 @@ kvq_status decode_impl(const kvq_cache* c, const kvq_decode_params* p, const voi
     if (probq) return KVQ_ERR_UNSUPPORTED;
     a.out_mult = c->k_scale;   // the values are the latent itself
     a.pe_scale_log2 = p->sm_scale * 1.4426950408889634f;
-    // four warps, each one 128-dim slice of the latent (64 code bytes) and a
-    // 16-dim slice of the rope key (32 bytes)
-    CUtensorMap tkv, tpe;
-    if (!make_slice_map(&tkv, c->k_codes, 64, 4, rows, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_slice_map(&tpe, c->k_pe, 32, 4, rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+    // latent codes as two 128-byte halves per row, rope keys as 128-byte rows,
+    // both in 16-row boxes with the 128-byte swizzle
+    // (and 64-row boxes for tiles inside one page)
+    CUtensorMap tkv, tpe, tkv64, tpe64;
+    if (!make_slice_map(&tkv, c->k_codes, 128, 2, rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_row_map(&tpe, c->k_pe, 128, rows) ||
+        !make_slice_map(&tkv64, c->k_codes, 128, 2, rows, CU_TENSOR_MAP_SWIZZLE_128B,
+                        rows >= 64 ? 64 : kBoxTokens) ||
+        !make_row_map(&tpe64, c->k_pe, 128, rows, rows >= 64 ? 64 : kBoxTokens))
       return KVQ_ERR_CUDA;
-    return cuda_status(launch_mla_partial(tkv, tpe, a, stream));
+    return cuda_status(launch_mla_partial(tkv, tpe, tkv64, tpe64, a, stream));
   }
   if (p->qk_dim != D || p->v_dim != D) return KVQ_ERR_INVALID;
   const bool ok_dims = (c->fmt == KVQ_FP8_E4M3 && (D == 64 || D == 128)) ||

@@ -180,6 +180,17 @@ __device__ __forceinline__ int obuf_swz(int head, int d) {
 
 // Output of one element in the requested type: fp32, bf16 (round to nearest
 // even) or the E4M3 code of fl32(o / out_scale).
+template <int DT>
+__device__ __forceinline__ void store_out_t(void* out, float out_scale, size_t i, float v) {
+  if constexpr (DT == 0) {
+    static_cast<float*>(out)[i] = v;
+  } else if constexpr (DT == 1) {
+    static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
+  } else {
+    static_cast<uint8_t*>(out)[i] = (uint8_t)(f32x2_to_e4m3x2(__fdiv_rn(v, out_scale), 0.f) & 0xFFu);
+  }
+}
+
 __device__ __forceinline__ void store_out(void* out, int dtype, float out_scale, size_t i, float v) {
   if (dtype == 0) {
     static_cast<float*>(out)[i] = v;
@@ -193,32 +204,77 @@ __device__ __forceinline__ void store_out(void* out, int dtype, float out_scale,
 // Merge of the s split partials of `rows` consecutive query heads starting at
 // partial row `row0` (M = max lse, w_j = e^(lse_j - M), O = sum w_j o_j /
 // sum w_j; O = 0 when every split is empty), written to `out` in the
-// requested type.  Each thread owns float4 columns (four consecutive value
-// dims of one row) and reads up to DEPTH splits of a column at once;
-// the loads of its first column are issued before the weights are known, so
-// that one memory round trip covers the lse and the partials.  One warp per
-// head row computes the weights (warp reductions).  w: rows *
-// kMaxFusedSplits floats of shared memory (s <= kMaxFusedSplits), winv: rows
-// floats.  The caller synchronizes before.
-template <int DEPTH = 32>
-__device__ __forceinline__ void merge_rows(const float* __restrict__ part_o,
-                                           const float* __restrict__ part_lse, size_t row0,
-                                           int rows, int s, int Dv, float* w, float* winv,
-                                           void* out, int out_dtype, float out_scale) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nq = Dv / 4;
-  const int items = rows * nq;
-  float4 v[DEPTH];
-  auto load = [&](int i, int j0) {
-    const float4* po =
-        reinterpret_cast<const float4*>(part_o + (row0 + i / nq) * (size_t)s * Dv) + i % nq;
+// requested type.  Threads own float4 columns (four consecutive value dims
+// of one row); one round of loads covers NI columns x NS splits (NI * NS =
+// DEPTH): one column at a time for many splits, several for few splits, so
+// that a thread's columns need few memory round trips.  The first round is
+// issued before the weights are known.  One warp per head row computes the
+// weights (warp reductions).  w: rows * kMaxFusedSplits floats of shared
+// memory (s <= kMaxFusedSplits), winv: rows floats.  The caller
+// synchronizes before.
+template <int NI, int NS>
+struct MergeRound {
+  float4 v[NI][NS];
+  __device__ __forceinline__ void load(const float* __restrict__ part_o, size_t row0, int s,
+                                       int nq, int items, int i, int j0) {
 #pragma unroll
-    for (int k = 0; k < DEPTH; ++k)
-      v[k] = j0 + k < s ? __ldcg(po + (size_t)(j0 + k) * nq) : make_float4(0.f, 0.f, 0.f, 0.f);
-  };
-  const int i0 = threadIdx.x;
-  if (i0 < items) load(i0, 0);
+    for (int u = 0; u < NI; ++u) {
+      const int it = i + u * (int)blockDim.x;
+      const float4* po =
+          reinterpret_cast<const float4*>(part_o + (row0 + it / nq) * (size_t)s * nq * 4) + it % nq;
+#pragma unroll
+      for (int k = 0; k < NS; ++k)
+        v[u][k] = (it < items && j0 + k < s) ? __ldcg(po + (size_t)(j0 + k) * nq)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+};
 
+template <int NI, int NS, int DT>
+__device__ __forceinline__ void merge_columns(const float* __restrict__ part_o, size_t row0,
+                                              int rows, int s, int Dv, const float* w,
+                                              const float* winv, void* out, float out_scale,
+                                              MergeRound<NI, NS>& rd, bool first_loaded) {
+  const int nq = Dv / 4, items = rows * nq, nt = blockDim.x;
+  for (int i = threadIdx.x; i < items; i += NI * nt) {
+    float4 acc[NI];
+#pragma unroll
+    for (int u = 0; u < NI; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 < s; j0 += NS) {
+      if (!(first_loaded && i == (int)threadIdx.x && j0 == 0))
+        rd.load(part_o, row0, s, nq, items, i, j0);
+#pragma unroll
+      for (int u = 0; u < NI; ++u) {
+        const int it = min(i + u * nt, items - 1);
+        const float* wr = w + (it / nq) * kMaxFusedSplits;
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+          const float wk = j0 + k < s ? wr[j0 + k] : 0.f;
+          acc[u].x += wk * rd.v[u][k].x;
+          acc[u].y += wk * rd.v[u][k].y;
+          acc[u].z += wk * rd.v[u][k].z;
+          acc[u].w += wk * rd.v[u][k].w;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < NI; ++u) {
+      const int it = i + u * nt;
+      if (it >= items) break;
+      const int r = it / nq;
+      const float iv = winv[r];
+      const size_t o = (row0 + r) * Dv + 4 * (it % nq);
+      store_out_t<DT>(out, out_scale, o + 0, acc[u].x * iv);
+      store_out_t<DT>(out, out_scale, o + 1, acc[u].y * iv);
+      store_out_t<DT>(out, out_scale, o + 2, acc[u].z * iv);
+      store_out_t<DT>(out, out_scale, o + 3, acc[u].w * iv);
+    }
+  }
+}
+
+__device__ __forceinline__ void merge_weights(const float* __restrict__ part_lse, size_t row0,
+                                              int rows, int s, float* w, float* winv) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int r = warp; r < rows; r += blockDim.x >> 5) {
     const float* lse = part_lse + (row0 + r) * s;
     float lv[kMaxFusedSplits / 32];
@@ -243,29 +299,39 @@ __device__ __forceinline__ void merge_rows(const float* __restrict__ part_o,
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (lane == 0) winv[r] = sum > 0.f ? 1.f / sum : (sum == 0.f ? 0.f : NAN);
   }
+}
+
+template <int NI, int NS>
+__device__ __forceinline__ void merge_rows_t(const float* __restrict__ part_o,
+                                             const float* __restrict__ part_lse, size_t row0,
+                                             int rows, int s, int Dv, float* w, float* winv,
+                                             void* out, int out_dtype, float out_scale) {
+  MergeRound<NI, NS> rd;
+  const int items = rows * (Dv / 4);
+  if ((int)threadIdx.x < items) rd.load(part_o, row0, s, Dv / 4, items, threadIdx.x, 0);
+  merge_weights(part_lse, row0, rows, s, w, winv);
   __syncthreads();
-  for (int i = i0; i < items; i += blockDim.x) {
-    const int r = i / nq;
-    const float* wr = w + r * kMaxFusedSplits;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j0 = 0; j0 < s; j0 += DEPTH) {
-      if (i != i0 || j0 != 0) load(i, j0);
-#pragma unroll
-      for (int k = 0; k < DEPTH; ++k) {
-        const float wk = j0 + k < s ? wr[j0 + k] : 0.f;
-        acc.x += wk * v[k].x;
-        acc.y += wk * v[k].y;
-        acc.z += wk * v[k].z;
-        acc.w += wk * v[k].w;
-      }
-    }
-    const float iv = winv[r];
-    const size_t o = (row0 + r) * Dv + 4 * (i % nq);
-    store_out(out, out_dtype, out_scale, o + 0, acc.x * iv);
-    store_out(out, out_dtype, out_scale, o + 1, acc.y * iv);
-    store_out(out, out_dtype, out_scale, o + 2, acc.z * iv);
-    store_out(out, out_dtype, out_scale, o + 3, acc.w * iv);
-  }
+  const bool first = (int)threadIdx.x < items;
+  if (out_dtype == 0)
+    merge_columns<NI, NS, 0>(part_o, row0, rows, s, Dv, w, winv, out, out_scale, rd, first);
+  else if (out_dtype == 1)
+    merge_columns<NI, NS, 1>(part_o, row0, rows, s, Dv, w, winv, out, out_scale, rd, first);
+  else
+    merge_columns<NI, NS, 2>(part_o, row0, rows, s, Dv, w, winv, out, out_scale, rd, first);
+}
+
+template <int DEPTH = 32>
+__device__ __forceinline__ void merge_rows(const float* __restrict__ part_o,
+                                           const float* __restrict__ part_lse, size_t row0,
+                                           int rows, int s, int Dv, float* w, float* winv,
+                                           void* out, int out_dtype, float out_scale) {
+  const int cols_per_thread = (rows * (Dv / 4) + (int)blockDim.x - 1) / (int)blockDim.x;
+  if (cols_per_thread >= 4 && 4 * s <= DEPTH)
+    merge_rows_t<4, DEPTH / 4>(part_o, part_lse, row0, rows, s, Dv, w, winv, out, out_dtype,
+                               out_scale);
+  else
+    merge_rows_t<1, DEPTH>(part_o, part_lse, row0, rows, s, Dv, w, winv, out, out_dtype,
+                           out_scale);
 }
 
 // Fused combine: the last CTA of a (request, kv head) to finish merges the
@@ -275,8 +341,10 @@ __device__ __forceinline__ void merge_rows(const float* __restrict__ part_o,
 // (made before the barrier) before the arrival, and in the last CTA its
 // acquire, extended to the CTA by the second barrier, makes every other
 // CTA's partials visible.  wbuf: kMaxGroup * (kMaxFusedSplits + 1) floats of
-// shared memory.  DEPTH: merge_rows' load depth (register budget).
-template <int DEPTH = 32>
+// shared memory.  DEPTH: loads in flight per thread (register budget); NI:
+// float4 columns per thread and round (several when a thread owns many
+// columns and s is small).
+template <int DEPTH = 32, int NI = 1>
 __device__ __forceinline__ void fused_combine(const PartialArgs& a, int bh, size_t part_row,
                                               float* wbuf) {
   __shared__ int is_last;
@@ -292,7 +360,7 @@ __device__ __forceinline__ void fused_combine(const PartialArgs& a, int bh, size
   }
   __syncthreads();
   if (!is_last) return;
-  merge_rows<DEPTH>(a.part_o, a.part_lse, part_row, a.G, a.num_splits, a.Dv, wbuf,
+  merge_rows_t<NI, DEPTH / NI>(a.part_o, a.part_lse, part_row, a.G, a.num_splits, a.Dv, wbuf,
              wbuf + kMaxGroup * kMaxFusedSplits, a.out, a.out_dtype, a.out_scale);
 }
 

@@ -100,7 +100,8 @@ struct TensorMaps {
 
 cudaError_t launch_partial(int fmt, int D, bool probq, const TensorMaps& m, const PartialArgs& a,
                            cudaStream_t st);
-cudaError_t launch_mla_partial(const CUtensorMap& tkv, const CUtensorMap& tpe,
+cudaError_t launch_mla_partial(const CUtensorMap& tcodes, const CUtensorMap& tpe,
+                               const CUtensorMap& tcodes64, const CUtensorMap& tpe64,
                                const PartialArgs& a, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 

@@ -1,4 +1,5 @@
-// MLA absorbed decode over an NVFP4 latent cache (sm_103a).
+// MLA absorbed decode over an NVFP4 latent cache on the 5th-generation tensor
+// cores (sm_103a: tcgen05 MMAs with accumulators in tensor memory).
 //
 // Model-Optimizer PR 714 (Testing: module printout) quantizes the MLA latent
 // cache kv_c (512 wide, after kv_a_layernorm) with an NVFP4 quantizer
@@ -7,22 +8,31 @@
 // 16 x 192).  Absorbed decode attends all 16 heads to one latent "kv head":
 //   S_i = sm_scale (q_lat . kv^_c,i + q_pe . k_pe,i),  V_i = kv^_c,i
 // with kv^_c the dequantized latent (e2m1 * block scale * global scale) and
-// k_pe the bf16 rope key (64 wide).  The split-KV scheme is the same as the
-// GQA kernel's (Model-Optimizer PR 1832 notes).
+// k_pe the bf16 rope key (64 wide).  The split-KV scheme is the GQA kernel's
+// (Model-Optimizer PR 1832 notes).
 //
-// GB300 design: four warps per CTA each own a 128-dim slice of the latent
-// (and one 16-dim slice of the rope key).  Per 16-token box:
-//  * each warp streams its own slice with TMA (3-D tensor maps: a 16 x 64 B
-//    code box and a 16 x 32 B rope box) plus the box's block-scale rows by a
-//    1-D bulk copy, through a private 4-deep mbarrier ring;
-//  * each warp computes a partial S^T = K Q^T over its slice on mma.sync
-//    (f16 latent fragments decoded from E2M1 * E4M3 exactly, bf16 rope
-//    fragments as stored); the four partials are summed through a small
-//    double-buffered shared-memory exchange (one CTA barrier per box);
-//  * every warp then runs the same softmax update (bitwise identical) and
-//    accumulates O^T = V^T P^T for its own 128 value dims, so the output
-//    needs no cross-warp merge.  P enters the MMA as f16 (N(0,1)-scale
-//    values keep its rounding far inside the tolerance; see the design notes).
+// GB300 design.  One CTA per SM runs one chunk in tiles of 64 tokens with
+// warp-specialized roles that hand work over through mbarriers:
+//  * a TMA warp streams each tile's latent codes (128-byte swizzled boxes),
+//    block scales (1-D bulk copy) and rope keys into a two-stage ring;
+//  * six decode warps turn a tile, once, into an f16 [token][dim] tile
+//    (E2M1 x E4M3 -> f16 is exact) in the 128-byte-swizzled layout that is
+//    the K-major A operand of S^T = K Q^T and, read MN-major, the A operand
+//    of O^T = V^T P^T; they copy the rope keys into a bf16 operand tile;
+//  * an MMA warp issues tcgen05.mma (kind::f16, M = 128, N = 16 heads): S^T
+//    of the latent (f16) and of the rope part (bf16) into two tensor-memory
+//    accumulators (their scales differ), O^T of four 128-dim blocks into a
+//    third, taking whichever tile is ready;
+//  * two softmax warps read S^T from tensor memory (one token per thread,
+//    all 16 heads), run the softmax with a lazily moving reference max and
+//    write P^T (f16) as the B operand of the O^T MMA.  When the reference
+//    max moves, O is rescaled in tensor memory by the four warps of the
+//    four lane sub-partitions (the softmax warps and decode warps 2-3).
+// Decoded tiles, rope tiles, S^T accumulators and P^T are double buffered.
+// The M = 128 S^T MMA over a 64-token tile also computes 64 rows from the
+// shared memory after the tile (always inside the allocation); they land in
+// tensor-memory lanes 64..127, which are never read.  Every wait is bounded;
+// a timeout sets an error bit and the partials become NaN.
 
 #include "kvq_attn.cuh"
 
@@ -33,30 +43,133 @@ constexpr int kMlaLat = 512;
 constexpr int kMlaRope = 64;
 constexpr int kMlaHeads = 16;
 constexpr int kMlaQkDim = kMlaLat + kMlaRope;
-constexpr int kSliceDims = kMlaLat / kDecodeWarps;   // 128 latent dims per warp
-constexpr int kScaleRow = kMlaLat / 16;              // 32 block-scale bytes per token
-constexpr int kMlaStages = 4;
-// per-warp stage: [codes 16 x 64 B][scale rows 16 x 32 B][rope 16 x 32 B]
-constexpr int kMlaCodeOff = 0, kMlaScaleOff = 1024, kMlaRopeOff = 1536, kMlaStage = 2048;
-constexpr int kMlaRing = kDecodeWarps * kMlaStages * kMlaStage;   // 32 KB
-// partial-score exchange: [2 box parities][4 warps][8 fragment regs][32 lanes]
-constexpr int kMlaSxFloats = 2 * kDecodeWarps * 8 * 32;
-constexpr int kMlaSmem = 1024 + kMlaRing + kMlaSxFloats * 4 + kMaxGroup * (kMaxFusedSplits + 1) * 4;
+constexpr int kT = 64;              // tokens per tile
+constexpr int kBoxes = kT / kBoxTokens;
+constexpr int kWorkers = 256;       // warps 0-1 softmax, 2-7 decode (2-3 also rescale O)
+constexpr int kDecoders = 192;      // warps 2-7
+constexpr int kMmaWarp = 8, kTmaWarp = 9;
+constexpr int kThreads = kWorkers + 64;
+constexpr int kTmemCols = 128;      // S lat [2] @0,16 | S rope [2] @32,48 | O^T 4 x 16 @64
+constexpr int kColSLat = 0, kColSPe = 32, kColO = 64;
+
+// shared-memory map (bytes from the 1024-aligned base); every MMA operand
+// tile starts on a 1024-byte boundary (the 128-byte swizzle period)
+constexpr int kTileBytes = kT * kMlaLat * 2;                  // f16 latent tile, 64 KB
+constexpr int kOffTile = 0;                                   // two tiles
+constexpr int kRawCodes = kT * kMlaLat / 2;                   // 16 KB: [half][64 rows x 128 B]
+constexpr int kRawScales = kT * (kMlaLat / 16);               // 2 KB block scales
+constexpr int kPeBytes = kT * kMlaRope * 2;                   // bf16 rope tile, 8 KB
+constexpr int kRawStage = kRawCodes + kRawScales + kPeBytes;  // codes | scales | rope keys
+constexpr int kRawStages = 2;
+constexpr int kOffRaw = kOffTile + 2 * kTileBytes;
+constexpr int kOffPe = kOffRaw + kRawStages * kRawStage;      // two rope operand tiles
+constexpr int kOffQLat = kOffPe + 2 * kPeBytes;               // f16 [16][512], 16 KB
+constexpr int kOffQPe = kOffQLat + kMlaHeads * kMlaLat * 2;   // bf16 [16][64], 2 KB
+constexpr int kPBytes = kMlaHeads * kT * 2;                   // f16 P^T [16][64], 2 KB
+constexpr int kOffP = kOffQPe + kMlaHeads * kMlaRope * 2;     // two P^T tiles
+constexpr int kSmemUsed = kOffP + 2 * kPBytes;
+constexpr int kSmemBytes = kSmemUsed + 1024;                  // alignment slack
+static_assert(kRawStage % 1024 == 0 && (kRawCodes + kRawScales) % 1024 == 0 && kOffPe % 1024 == 0 && kOffQLat % 1024 == 0 &&
+                  kOffQPe % 1024 == 0 && kOffP % 1024 == 0,
+              "operand tiles on the swizzle period");
+// the S^T MMA reads 128 rows (16 KB per 64-dim column of atoms) of a 64-row
+// tile: the extra 8 KB after the last tile and the last rope tile stay inside
+static_assert(kOffTile + 2 * kTileBytes + 8192 <= kSmemUsed, "tile over-read in bounds");
+static_assert(kOffPe + 2 * kPeBytes + 8192 <= kSmemUsed, "rope over-read in bounds");
+static_assert(kRawStages * kRawStage >= kMaxGroup * (kMaxFusedSplits + 1) * 4,
+              "combine weights fit in the raw ring");
 
 struct MlaSmem {
-  uint64_t full[kDecodeWarps][kMlaStages];
+  uint64_t raw_full[kRawStages];   // codes, scales and rope keys of a tile landed
+  uint64_t s_done[2];              // S^T MMAs of a tile completed
+  uint64_t o_done[2];              // O^T MMAs of a tile completed
+  uint64_t dec_ready[2];           // decode warps: tile decoded (operands visible)
+  uint64_t p_done[2];              // softmax warps: P^T and the rescale decision written
+  uint64_t p_ready[2];             // P^T written and O rescaled: O^T MMA may go
+  uint64_t resc_done;              // warps 2-3: their half of an O rescale is done
+  uint64_t comb_full;              // fused combine: partials landed
+  uint32_t tmem;                   // tensor-memory base address
   int abort_flag;
+  int rescale[2];                  // tile parity: O must be rescaled before O^T MMA t
+  int need[2];                     // softmax warps: the reference max must move
+  float alpha[2][kMlaHeads];       // tile parity: O rescale factors
+  float wmax[2][kMlaHeads];        // per-warp tile maxima
+  float lsum[2][kMlaHeads];        // per-warp denominators (end)
+  float m[kMlaHeads];              // final reference max (end)
   int pages[kPageCache];
-  float lse[kMlaHeads];
 };
 
-// Column swizzle of the output buffer [head][512]: XOR-ing the low four bits
-// of d with (lane group / 2, head pair) makes the fragment stores and the
-// row-wise reads conflict-free.
-__device__ __forceinline__ int mla_swz(int head, int d) {
-  return d ^ (((d >> 5) & 3) | (((head >> 1) & 3) << 2));
+// ----------------------------------------------------------------- tcgen05
+// Shared-memory matrix descriptor: start, leading/stride byte offsets (16-byte
+// units), descriptor version 1, 128-byte swizzle.  K-major operands: SBO =
+// distance of 8-row groups; MN-major: LBO = distance of 64-element columns
+// along M/N, SBO = distance of 8-row groups along K.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
+// Instruction descriptor, kind::f16: D f32, A/B f16 (0) or bf16 (1), A K-major
+// (0) or MN-major (1), B K-major, N = 16, M = 128.
+__host__ __device__ constexpr uint32_t idesc(uint32_t ab_fmt, uint32_t a_mn) {
+  return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | (a_mn << 15) | ((16u >> 3) << 17) |
+         ((128u >> 4) << 24);
+}
+constexpr uint32_t kIdF16 = idesc(0, 0), kIdBf16 = idesc(1, 0), kIdF16MnA = idesc(0, 1);
 
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                    bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(id), "r"((uint32_t)acc)
+      : "memory");
+}
+// arrives on `bar` once every MMA this thread issued before has completed
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 32 lanes x 16 columns of 32 bits: thread i of the warp gets lane (base + i)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                       uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z,
                                             uint32_t bar) {
   asm volatile(
@@ -66,57 +179,169 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
-__global__ void __launch_bounds__(kDecodeThreads, 2)
-    mla_partial_kernel(const __grid_constant__ CUtensorMap tmKv,
-                       const __grid_constant__ CUtensorMap tmPe, const PartialArgs a) {
-  using Gs = Geom<kFmtNvfp4, kSliceDims>;   // a warp's slice looks like an NVFP4 D=128 row
-  constexpr int KS = kSliceDims / 16;       // 8 latent k-steps per warp
-  constexpr int MT = kSliceDims / 16;       // 8 value m-tiles per warp
+// byte offset of 16-bit element (row r, col c < 64) in a 128-byte-swizzled
+// column of 8-row atoms (atom stride 1 KB)
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((c >> 3) ^ r) & 7) << 4) + (c & 7) * 2);
+}
 
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait by the calling thread; a timeout raises the CTA's abort flag.
+__device__ __forceinline__ void wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (!mbar_wait(bar, parity)) *abort_flag = 1;
+}
+
+// Weighted sum of the s staged partials [16][s][512] (shared memory) into
+// the output, four value dims per thread and step.
+template <int DT>
+__device__ __forceinline__ void mla_merge_smem(const PartialArgs& a, size_t part_row, int s,
+                                               const uint8_t* staged, const float* w,
+                                               const float* winv, bool ok) {
+  const float4* po = reinterpret_cast<const float4*>(staged);
+  constexpr int nq = kMlaLat / 4;
+#pragma unroll 1
+  for (int i = threadIdx.x; i < kMlaHeads * nq; i += blockDim.x) {
+    const int r = i / nq, d4 = i % nq;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int j = 0; j < s; ++j) {
+      const float wj = w[r * kMaxFusedSplits + j];
+      const float4 v = po[(r * s + j) * nq + d4];
+      acc.x += wj * v.x;
+      acc.y += wj * v.y;
+      acc.z += wj * v.z;
+      acc.w += wj * v.w;
+    }
+    const float iv = ok ? winv[r] : NAN;
+    const size_t o = (part_row + r) * kMlaLat + 4 * d4;
+    store_out_t<DT>(a.out, a.out_scale, o + 0, acc.x * iv);
+    store_out_t<DT>(a.out, a.out_scale, o + 1, acc.y * iv);
+    store_out_t<DT>(a.out, a.out_scale, o + 2, acc.z * iv);
+    store_out_t<DT>(a.out, a.out_scale, o + 3, acc.w * iv);
+  }
+}
+
+// Fused combine of the MLA kernel: the last CTA of a request merges the s
+// partials of its 16 heads.  With s <= 4 the partials (16 x s x 512 floats,
+// contiguous) come into shared memory with one bulk copy and are summed by a
+// short loop; otherwise the general merge runs.  The arrival protocol is the
+// GQA kernel's (one acq_rel atomic after a CTA barrier).
+__device__ __forceinline__ void mla_fused_combine(const PartialArgs& a, int b, size_t part_row,
+                                                  uint32_t base, uint8_t* gbase, uint32_t bar) {
+  __shared__ int is_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(prev)
+                 : "l"(a.counters + b)
+                 : "memory");
+    is_last = prev == (unsigned)(a.num_splits - 1);
+    if (is_last) a.counters[b] = 0u;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  const int s = a.num_splits;
+  float* wbuf = reinterpret_cast<float*>(gbase + kOffRaw);
+  float* winv = wbuf + kMaxGroup * kMaxFusedSplits;
+  if (s > 4) {
+    merge_rows_t<4, 8>(a.part_o, a.part_lse, part_row, kMlaHeads, s, kMlaLat, wbuf, winv, a.out,
+                       a.out_dtype, a.out_scale);
+    return;
+  }
+  const uint32_t bytes = (uint32_t)(kMlaHeads * s * kMlaLat * 4);   // <= 128 KB: the two tiles
+  if (threadIdx.x == 0) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");   // acquired data -> bulk copy
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_load(base + kOffTile, a.part_o + part_row * s * kMlaLat, bytes, bar);
+  }
+  merge_weights(a.part_lse, part_row, kMlaHeads, s, wbuf, winv);
+  const bool ok = mbar_wait(bar, 0);
+  __syncthreads();
+  if (a.out_dtype == 0)          // fp32
+    mla_merge_smem<0>(a, part_row, s, gbase + kOffTile, wbuf, winv, ok);
+  else if (a.out_dtype == 1)     // bf16
+    mla_merge_smem<1>(a, part_row, s, gbase + kOffTile, wbuf, winv, ok);
+  else
+    mla_merge_smem<2>(a, part_row, s, gbase + kOffTile, wbuf, winv, ok);
+  if (!ok && threadIdx.x == 0) record_error(a.error_flag, 1);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_tc_kernel(const __grid_constant__ CUtensorMap tmCodes,
+                  const __grid_constant__ CUtensorMap tmPe,
+                  const __grid_constant__ CUtensorMap tmCodes64,
+                  const __grid_constant__ CUtensorMap tmPe64, const PartialArgs a) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ MlaSmem sm;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x, split = blockIdx.y;
+  const uint32_t base = (smem_u32(dyn_smem) + 1023u) & ~1023u;
+  uint8_t* gbase = dyn_smem + (base - smem_u32(dyn_smem));
+  volatile int* abort_flag = &sm.abort_flag;
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int b = blockIdx.x;
-  const int split = blockIdx.y;
-
-  const uint32_t ring = (smem_u32(dyn_smem) + 1023u) & ~1023u;
-  float* sx = reinterpret_cast<float*>(dyn_smem + (ring - smem_u32(dyn_smem)) + kMlaRing);
-  float* wbuf = sx + kMlaSxFloats;
-
-  const int cap = min(a.max_pages * a.ps, a.max_kv_len);
-  // only barrier setup before the grid-dependency wait
-  if (threadIdx.x == 0) sm.abort_flag = 0;
-  if (lane == 0) {
-    for (int i = 0; i < kMlaStages; ++i) mbar_init(smem_u32(&sm.full[warp][i]), 1);
+  // ---- setup that reads no input: barriers, tensor memory
+  if (tid == 0) {
+    for (int i = 0; i < kRawStages; ++i) mbar_init(smem_u32(&sm.raw_full[i]), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sm.s_done[i]), 1);
+      mbar_init(smem_u32(&sm.o_done[i]), 1);
+      mbar_init(smem_u32(&sm.dec_ready[i]), kDecoders);
+      mbar_init(smem_u32(&sm.p_done[i]), 1);
+      mbar_init(smem_u32(&sm.p_ready[i]), 1);
+    }
+    mbar_init(smem_u32(&sm.resc_done), 64);
+    mbar_init(smem_u32(&sm.comb_full), 1);
+    sm.abort_flag = 0;
+    sm.rescale[0] = sm.rescale[1] = 0;
     fence_barrier_init();
-  }
-  if (threadIdx.x == 32) {
-    prefetch_tmap(&tmKv);
+    prefetch_tmap(&tmCodes);
     prefetch_tmap(&tmPe);
+    prefetch_tmap(&tmCodes64);
+    prefetch_tmap(&tmPe64);
   }
-  // overlap mode (a.fresh > 0): only the loads of boxes that hold the last
-  // a.fresh positions wait for the preceding append
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sm.tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // overlap mode (a.fresh > 0): only loads of tiles holding the last a.fresh
+  // positions wait for the preceding append
   if (a.fresh == 0) griddep_wait();
 
+  // ---- chunk of this split
   int L = a.seq_lens[b];
+  const int cap = min(a.max_pages * a.ps, a.max_kv_len);
   if (L > cap || L < 0) {
-    if (threadIdx.x == 0) record_error(a.error_flag, 2);
+    if (tid == 0) record_error(a.error_flag, 2);
     L = L < 0 ? 0 : cap;
   }
   long c = ((long)L + a.num_splits - 1) / a.num_splits;
   c = (c + 15) / 16 * 16;
   const int cstart = (int)min((long)split * c, (long)L);
   const int cend = (int)min((long)cstart + c, (long)L);
-  const int nboxes = (cend - cstart + kBoxTokens - 1) / kBoxTokens;   // all warps, all boxes
-  const int fresh_box = a.fresh == 0 ? 0 : (max(L - a.fresh, cstart) - cstart) / kBoxTokens;
-  bool dep_done = a.fresh == 0;
+  const int ntok = cend - cstart;
+  const int nt = (ntok + kT - 1) / kT;
+  const int fresh_tok = a.fresh == 0 ? 0x7fffffff : max(L - a.fresh, cstart) - cstart;
+  bool dep_done = a.fresh == 0;   // issuer: has waited for the preceding kernel
 
   const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
   const int p0 = cstart / a.ps;
   const int npages = cend > cstart ? (cend - 1) / a.ps - p0 + 1 : 0;
-  for (int i = threadIdx.x; i < min(npages, kPageCache); i += kDecodeThreads) {
+  for (int i = tid; i < min(npages, kPageCache); i += kThreads) {
     int pg = __ldg(bt + p0 + i);
     if (pg < 0 || pg >= a.num_pages) {
       record_error(a.error_flag, 4);
@@ -124,12 +349,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     }
     sm.pages[i] = pg;
   }
-  __syncthreads();
-  volatile int* abort_flag = &sm.abort_flag;
 
-  // this warp's slice of box j: codes, all block-scale rows, rope slice
-  auto issue = [&](int j) {
-    const int tok = cstart + j * kBoxTokens;
+  tc_fence_before();
+  __syncthreads();   // page cache and tensor-memory address ready
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+
+  auto cache_row = [&](int tok) -> long {
     const int pidx = tok / a.ps;
     int page;
     if (pidx - p0 < kPageCache) {
@@ -141,233 +367,391 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
         page = 0;
       }
     }
-    const long row = (long)page * a.ps + (tok % a.ps);
-    if (!dep_done && j >= fresh_box) {
-      griddep_wait();
-      dep_done = true;
-    }
-    const int st = j % kMlaStages;
-    const uint32_t full = smem_u32(&sm.full[warp][st]);
-    const uint32_t sbase = ring + (warp * kMlaStages + st) * kMlaStage;
-    mbar_arrive_expect_tx(full, 16 * 64 + 16 * kScaleRow + 16 * 32);
-    tma_load_3d(sbase + kMlaCodeOff, &tmKv, 0, warp, (int)row, full);
-    bulk_load(sbase + kMlaScaleOff, a.k_bscale + row * kScaleRow, 16 * kScaleRow, full);
-    tma_load_3d(sbase + kMlaRopeOff, &tmPe, 0, warp, (int)row, full);
+    return (long)page * a.ps + (tok % a.ps);
   };
-  int issued = 0;
-  if (lane == 0)
-    for (; issued < min(nboxes, kMlaStages); ++issued) issue(issued);
 
-  // Q^T fragments: latent dims 128 w + 32 t + 4 j + {0..3} (permuted like
-  // the K fragments) and rope dims 512 + 16 w + 4 t + {0..3} (bf16 as is)
-  uint32_t qb[KS][2][2], qr[2][2];
+  // softmax state (warps 0, 1: one token per thread, all 16 heads)
+  float m[kMlaHeads], l[kMlaHeads];
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    const uint16_t* qh = a.q + ((size_t)b * kMlaHeads + g + 8 * hh) * kMlaQkDim;
-    const uint16_t* qp = qh + kSliceDims * warp + 32 * t;
-#pragma unroll
-    for (int j = 0; j < KS; ++j) {
-      const uint2 v = *reinterpret_cast<const uint2*>(qp + 4 * j);
-      qb[j][hh][0] = pack_f16x2(bf16_bits_to_f32(v.x & 0xFFFFu), bf16_bits_to_f32(v.x >> 16));
-      qb[j][hh][1] = pack_f16x2(bf16_bits_to_f32(v.y & 0xFFFFu), bf16_bits_to_f32(v.y >> 16));
-    }
-    const uint2 r = *reinterpret_cast<const uint2*>(qh + kMlaLat + 16 * warp + 4 * t);
-    qr[hh][0] = r.x;
-    qr[hh][1] = r.y;
-  }
+  for (int h = 0; h < kMlaHeads; ++h) m[h] = -INFINITY, l[h] = 0.f;
 
-  float o[MT][2][4];
-#pragma unroll
-  for (int i = 0; i < MT; ++i)
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) o[i][hh][0] = o[i][hh][1] = o[i][hh][2] = o[i][hh][3] = 0.f;
-  float m[2][2], l[2][2];
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) m[hh][0] = m[hh][1] = -INFINITY, l[hh][0] = l[hh][1] = 0.f;
-  bool aborted = false;
-
-  for (int j = 0; j < nboxes; ++j) {
-    const int st = j % kMlaStages;
-    // Every warp takes part in the per-box barrier, so a failed wait does
-    // not leave the loop: the warp skips its work and keeps step.
-    if (!aborted) {
-      bool got = true;
-      if (lane == 0)
-        got = wait_or_abort(smem_u32(&sm.full[warp][st]), (j / kMlaStages) & 1, abort_flag);
-      aborted = !__all_sync(0xffffffffu, got);
-      __syncwarp();
-    }
-    const int tbase = cstart + j * kBoxTokens;
-    const int nvalid = min(kBoxTokens, cend - tbase);
-    const uint32_t sbase = ring + (warp * kMlaStages + st) * kMlaStage;
-    const uint32_t boxK = sbase + kMlaCodeOff;
-    const uint32_t boxS = sbase + kMlaScaleOff + 8 * warp;   // this slice's 8 blocks of a row
-    float* sxp = sx + (j & 1) * (kDecodeWarps * 8 * 32);
-
-    if (!aborted) {
-      // ---- partial scores of this warp's slice (log2 domain, scaled)
-      uint32_t kg[KS][2], kg8[KS][2];
-      k_frag<kFmtNvfp4, kSliceDims, kScaleRow>(boxK, boxS, g, t, kg);
-      k_frag<kFmtNvfp4, kSliceDims, kScaleRow>(boxK, boxS, g + 8, t, kg8);
-      const uint2 rg = lds64(sbase + kMlaRopeOff + g * 32 + 8 * t);
-      const uint2 rg8 = lds64(sbase + kMlaRopeOff + (g + 8) * 32 + 8 * t);
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-        float sp[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kk = 0; kk < KS; kk += 2) {
-          mma_f16(s0, kg[kk][0], kg8[kk][0], kg[kk][1], kg8[kk][1], qb[kk][hh][0], qb[kk][hh][1]);
-          mma_f16(s1, kg[kk + 1][0], kg8[kk + 1][0], kg[kk + 1][1], kg8[kk + 1][1],
-                  qb[kk + 1][hh][0], qb[kk + 1][hh][1]);
+  // ============================================================ TMA warp
+  if (warp == kTmaWarp) {
+    if (lane == 0) {
+      auto fresh_wait = [&](int x) {
+        if (!dep_done && x * kT + kT > fresh_tok) {
+          griddep_wait();
+          dep_done = true;
         }
-        mma_bf16(sp, rg.x, rg8.x, rg.y, rg8.y, qr[hh][0], qr[hh][1]);
+      };
+      // A tile inside one page moves as four copies (64-row boxes), otherwise
+      // as four per 16-token box.  Stage layout: codes [half][row][128 B]
+      // (128-byte swizzle), scales [row][32 B], rope keys [row][128 B].
+      auto issue_raw = [&](int x) {
+        fresh_wait(x);
+        const int nb = min(kBoxes, (ntok - x * kT + kBoxTokens - 1) / kBoxTokens);
+        const uint32_t st = base + kOffRaw + (x % kRawStages) * kRawStage;
+        const uint32_t bar = smem_u32(&sm.raw_full[x % kRawStages]);
+        constexpr uint32_t kRowBytes = kMlaLat / 2 + kMlaLat / 16 + kMlaRope * 2;   // 416
+        mbar_arrive_expect_tx(bar, nb * kBoxTokens * kRowBytes);
+        const int tok0 = cstart + x * kT;
+        const long row0 = cache_row(tok0);
+        if (nb == kBoxes && tok0 / a.ps == (tok0 + kT - 1) / a.ps) {
+          tma_load_3d(st, &tmCodes64, 0, 0, (int)row0, bar);
+          tma_load_3d(st + kRawCodes / 2, &tmCodes64, 0, 1, (int)row0, bar);
+          bulk_load(st + kRawCodes, a.k_bscale + row0 * (kMlaLat / 16), kT * (kMlaLat / 16), bar);
+          tma_load_2d(st + kRawCodes + kRawScales, &tmPe64, 0, (int)row0, bar);
+          return;
+        }
+        for (int k = 0; k < nb; ++k) {
+          const long row = k == 0 ? row0 : cache_row(tok0 + k * kBoxTokens);
+          tma_load_3d(st + k * 2048, &tmCodes, 0, 0, (int)row, bar);
+          tma_load_3d(st + kRawCodes / 2 + k * 2048, &tmCodes, 0, 1, (int)row, bar);
+          bulk_load(st + kRawCodes + k * (kBoxTokens * (kMlaLat / 16)),
+                    a.k_bscale + row * (kMlaLat / 16), kBoxTokens * (kMlaLat / 16), bar);
+          tma_load_2d(st + kRawCodes + kRawScales + k * 2048, &tmPe, 0, (int)row, bar);
+        }
+      };
+      int issued = 0;
+      for (; issued < nt; ++issued) {
+        // the stage of tile x was read by the decode of tile x - 2
+        if (issued >= kRawStages)
+          wait_bar(smem_u32(&sm.dec_ready[issued & 1]), ((issued - kRawStages) >> 1) & 1,
+                   abort_flag);
+        if (*abort_flag) break;
+        issue_raw(issued);
+      }
+      if (!dep_done) griddep_wait();   // the grid ends after the append it overlapped
+      for (int x = max(0, issued - kRawStages); x < issued; ++x)
+        mbar_wait(smem_u32(&sm.raw_full[x % kRawStages]), (x / kRawStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ========================================================== MMA warp
+    int s_next = 0, o_next = 0;
+    if (lane == 0) {
+      // Descriptors are built once; per MMA only the start-address field
+      // moves (16-byte units, no carry out of 14 bits: every shared address
+      // is below 256 KB).
+      const uint64_t dq = sdesc(base + kOffQLat, 16, 1024);
+      const uint64_t dqpe = sdesc(base + kOffQPe, 16, 1024);
+      auto issue_s = [&](int x) {
+        const uint64_t da = sdesc(base + kOffTile + (x & 1) * kTileBytes, 16, 1024);
+        const uint64_t dpe = sdesc(base + kOffPe + (x & 1) * kPeBytes, 16, 1024);
+        const uint32_t dl = tmem + kColSLat + 16 * (x & 1), dp = tmem + kColSPe + 16 * (x & 1);
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sxp[(warp * 8 + 4 * hh + e) * 32 + lane] =
-              (s0[e] + s1[e]) * a.qk_scale_log2 + sp[e] * a.pe_scale_log2;
+        for (int kk = 0; kk < kMlaLat / 16; ++kk)
+          mma(dl, da + (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4),
+              dq + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), kIdF16, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kMlaRope / 16; ++kk)
+          mma(dp, dpe + (uint64_t)(kk * 2), dqpe + (uint64_t)(kk * 2), kIdBf16, kk > 0);
+        mma_commit(smem_u32(&sm.s_done[x & 1]));
+      };
+      auto issue_o = [&](int x) {
+        const uint64_t da = sdesc(base + kOffTile + (x & 1) * kTileBytes, 8192, 1024);
+        const uint64_t dpt = sdesc(base + kOffP + (x & 1) * kPBytes, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+#pragma unroll
+          for (int i = 0; i < kMlaLat / 128; ++i)
+            mma(tmem + kColO + 16 * i, da + (uint64_t)(((2 * i) * 8192 + (2 * kk) * 1024) >> 4),
+                dpt + (uint64_t)(kk * 2), kIdF16MnA, x > 0 || kk > 0);
+        mma_commit(smem_u32(&sm.o_done[x & 1]));
+      };
+      // S^T MMA x: tile x decoded, and its S^T buffer read by the softmax of
+      // x-2 (whose P^T made O^T x-2 issuable); O^T MMA x: P^T x written (and
+      // O rescaled).  Whichever is ready goes first; the O^T MMA is preferred
+      // (the decode of tile x+2 waits for it).
+      uint64_t t0 = globaltimer_ns();
+      while (o_next < nt && !*abort_flag) {
+        if (o_next < s_next &&
+            mbar_test(smem_u32(&sm.p_ready[o_next & 1]), (o_next >> 1) & 1)) {
+          tc_fence_after();
+          issue_o(o_next);
+          ++o_next;
+          t0 = globaltimer_ns();
+        } else if (s_next < nt && s_next <= o_next + 1 &&
+                   mbar_test(smem_u32(&sm.dec_ready[s_next & 1]), (s_next >> 1) & 1)) {
+          tc_fence_after();
+          issue_s(s_next);
+          ++s_next;
+          t0 = globaltimer_ns();
+        } else if (globaltimer_ns() - t0 > 250000000ull) {
+          *abort_flag = 1;
+        }
+      }
+      // every MMA issued has completed (bounded waits)
+      for (int x = max(0, s_next - 2); x < s_next; ++x)
+        mbar_wait(smem_u32(&sm.s_done[x & 1]), (x >> 1) & 1);
+      bool ok = true;
+      for (int x = max(0, o_next - 2); x < o_next; ++x)
+        ok &= mbar_wait(smem_u32(&sm.o_done[x & 1]), (x >> 1) & 1);
+      if (!ok || o_next < nt) *abort_flag = 1;
+    }
+    __syncwarp();
+  } else {
+    // ============================================================ workers
+    // Q (decode warps): latent part as f16 (K-major [16 heads][512], 64-dim
+    // atom columns 2 KB apart), rope part as bf16 ([16][64])
+    const int dt = tid - 64;   // decode thread 0..191
+    if (warp >= 2) {
+      const uint16_t* qg = a.q + (size_t)b * kMlaHeads * kMlaQkDim;
+      for (int i = dt; i < kMlaHeads * (kMlaQkDim / 8); i += kDecoders) {
+        const int h = i / (kMlaQkDim / 8), d = (i % (kMlaQkDim / 8)) * 8;
+        const uint4 v = *reinterpret_cast<const uint4*>(qg + (size_t)h * kMlaQkDim + d);
+        if (d < kMlaLat) {
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          uint32_t f[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            f[k] = pack_f16x2(bf16_bits_to_f32(w[k] & 0xFFFFu), bf16_bits_to_f32(w[k] >> 16));
+          sts128(base + kOffQLat + (d >> 6) * 2048 + swz(h, d & 63), f[0], f[1], f[2], f[3]);
+        } else {
+          sts128(base + kOffQPe + swz(h, d - kMlaLat), v.x, v.y, v.z, v.w);
+        }
       }
     }
-    __syncthreads();   // the four slice partials of this box are in shared memory
-    if (!aborted) {
-      float x[2][4];
+    // Decode of tile x into tile buffer x % 2 (decode warps).  A unit is
+    // (token, 64-dim column, half) = 32 dims; eight consecutive threads take
+    // the eight tokens of an atom, so that the swizzled loads and stores
+    // spread over all banks.  Rows past the chunk are zero (finite operands
+    // for the masked tokens of the O^T MMA).  The rope keys move unchanged
+    // (same swizzled layout in the stage and in the operand tile).
+    auto decode = [&](int x) {
+      const uint32_t st = base + kOffRaw + (x % kRawStages) * kRawStage;
+      const uint32_t tile = base + kOffTile + (x & 1) * kTileBytes;
+      const int nvalid = min(kT, ntok - x * kT);
+#pragma unroll 1
+      for (int u = dt; u < kT * 16; u += kDecoders) {
+        const int p = u & 7, rest = u >> 3;
+        const int rg = rest >> 4, db = (rest & 15) >> 1, half = rest & 1;
+        const int r = rg * 8 + p;
+        uint32_t o[4][4];
+        if (r < nvalid) {
+          const uint4 v = lds128(st + (db >> 2) * (kRawCodes / 2) + r * 128 +
+                                 (((((db & 3) * 2 + half) ^ r) & 7) << 4));
+          const uint32_t sc = lds16(st + kRawCodes + r * (kMlaLat / 16) + db * 4 + half * 2);
+          const uint32_t s2 = e4m3x2_to_f16x2(sc);
+          const uint32_t s_lo = __byte_perm(s2, 0, 0x1010), s_hi = __byte_perm(s2, 0, 0x3232);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float v = 0.f;
-#pragma unroll
-          for (int w = 0; w < kDecodeWarps; ++w) v += sxp[(w * 8 + 4 * hh + e) * 32 + lane];
-          x[hh][e] = (g + 8 * (e >> 1) < nvalid) ? v : -INFINITY;
-        }
-      // ---- softmax update with a lazily moving reference max (identical in
-      // every warp: same inputs, same operations)
-      bool need = false;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) need |= x[hh][e] > m[hh][e & 1] + 8.0f;
-      if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float mx = fmaxf(x[hh][e], x[hh][e + 2]);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const bool mv = mx > m[hh][e] + 8.0f;
-            const float alpha = mv ? ex2(m[hh][e] - mx) : 1.f;
-            m[hh][e] = mv ? mx : m[hh][e];
-            l[hh][e] *= alpha;
-#pragma unroll
-            for (int i = 0; i < MT; ++i) {
-              o[i][hh][e] *= alpha;
-              o[i][hh][e + 2] *= alpha;
-            }
+          for (int k = 0; k < 4; ++k) {
+            uint32_t e0, e1, e2, e3;
+            e2m1x8_to_f16x2x4(w[k], e0, e1, e2, e3);
+            const uint32_t s = k < 2 ? s_lo : s_hi;
+            o[k][0] = hmul2(e0, s);
+            o[k][1] = hmul2(e1, s);
+            o[k][2] = hmul2(e2, s);
+            o[k][3] = hmul2(e3, s);
           }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0u;
+        }
+        const uint32_t row_base = tile + db * 8192 + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          sts128(row_base + ((((half * 4 + k) ^ r) & 7) << 4), o[k][0], o[k][1], o[k][2],
+                 o[k][3]);
       }
-      uint32_t pb[2][2];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const float b0 = m[hh][0] == -INFINITY ? 0.f : m[hh][0];
-        const float b1 = m[hh][1] == -INFINITY ? 0.f : m[hh][1];
-        const float p0 = ex2(x[hh][0] - b0), p1 = ex2(x[hh][1] - b1);
-        const float p2 = ex2(x[hh][2] - b0), p3 = ex2(x[hh][3] - b1);
-        l[hh][0] += p0 + p2;
-        l[hh][1] += p1 + p3;
-        pb[hh][0] = movmatrix_trans(pack_f16x2(p0, p1));
-        pb[hh][1] = movmatrix_trans(pack_f16x2(p2, p3));
+      const uint32_t pe_src = st + kRawCodes + kRawScales;
+      const uint32_t pe_dst = base + kOffPe + (x & 1) * kPeBytes;
+#pragma unroll 1
+      for (int i = dt; i < kPeBytes / 16; i += kDecoders) {
+        const uint4 v = lds128(pe_src + i * 16);
+        sts128(pe_dst + i * 16, v.x, v.y, v.z, v.w);
       }
-      // ---- O^T += V^T P^T over this warp's 128 value dims (V = the latent)
-      uint32_t va[MT][4];
-      v_frag<kFmtNvfp4, kSliceDims, kScaleRow>(boxK, boxS, t, g, nvalid, va);
-#pragma unroll
-      for (int i = 0; i < MT; ++i)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-          mma_f16(o[i][hh], va[i][0], va[i][1], va[i][2], va[i][3], pb[hh][0], pb[hh][1]);
-      __syncwarp();
-      if (lane == 0 && issued < nboxes) {
-        fence_proxy_async_shared();
-        issue(issued++);
-      }
-    }
-  }
-  if (aborted) {
-    *abort_flag = 1;
-    record_error(a.error_flag, 1);
-  }
-  if (lane == 0) {
-    const int done = aborted ? 0 : nboxes;
-    for (int k = max(done, issued - kMlaStages); k < issued; ++k)
-      mbar_wait(smem_u32(&sm.full[warp][k % kMlaStages]), (k / kMlaStages) & 1);
-  }
-  __syncwarp();
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float v = l[hh][e];
-      v += __shfl_xor_sync(0xffffffffu, v, 4);
-      v += __shfl_xor_sync(0xffffffffu, v, 8);
-      v += __shfl_xor_sync(0xffffffffu, v, 16);
-      l[hh][e] = v;
-    }
-  __syncthreads();
-  if (!dep_done && threadIdx.x == 0) griddep_wait();   // the grid ends after the append
-  const bool bad = *abort_flag != 0;
-  // normalized O of this warp's dims -> shared memory obuf[head][512] (the ring
-  // is drained), then coalesced stores of the partials
-  float* obuf = reinterpret_cast<float*>(dyn_smem + (ring - smem_u32(dyn_smem)));
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int head = 2 * t + (e & 1) + 8 * hh;
-      const float li = l[hh][e & 1];
-      const float f = (li > 0.f) ? a.out_mult / li : 0.f;
-#pragma unroll
-      for (int i = 0; i < MT; ++i) {
-        const int d = kSliceDims * warp + 16 * g + 2 * i + (e >> 1);
-        obuf[head * kMlaLat + mla_swz(head, d)] = bad ? NAN : o[i][hh][e] * f;
-      }
-    }
-  if (warp == 0 && g == 0) {
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float mm = m[hh][e], li = l[hh][e];
-        sm.lse[2 * t + e + 8 * hh] = bad ? NAN : (mm == -INFINITY || li == 0.f) ? -INFINITY
-                                                                               : (mm + log2f(li)) * kLn2;
-      }
-  }
-  __syncthreads();
-  const size_t part_row = (size_t)b * kMlaHeads;
-  for (int i = threadIdx.x; i < kMlaHeads * kMlaLat; i += kDecodeThreads) {
-    const int head = i / kMlaLat, d = i % kMlaLat;
-    a.part_o[((part_row + head) * a.num_splits + split) * kMlaLat + d] =
-        obuf[head * kMlaLat + mla_swz(head, d)];
-  }
-  if (threadIdx.x < kMlaHeads)
-    a.part_lse[(part_row + threadIdx.x) * a.num_splits + split] = sm.lse[threadIdx.x];
-  if (a.counters) fused_combine(a, b, part_row, wbuf);
-}
+      fence_proxy_async_shared();   // generic stores -> operands of the async MMAs
+      mbar_arrive(smem_u32(&sm.dec_ready[x & 1]));
+    };
 
+    // O rescale of the 32 tensor-memory lanes of this warp's sub-partition
+    // (the reference max of some heads moved at tile t; O^T MMA t-1 done)
+    auto rescale_o = [&](int t) {
+      wait_bar(smem_u32(&sm.o_done[(t - 1) & 1]), ((t - 1) >> 1) & 1, abort_flag);
+      tc_fence_after();
+      const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+#pragma unroll 1
+      for (int i = 0; i < kMlaLat / 128; ++i) {
+        uint32_t v[16];
+        tmem_ld16(lane_addr + kColO + 16 * i, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < kMlaHeads; ++h)
+          v[h] = __float_as_uint(__uint_as_float(v[h]) * sm.alpha[t & 1][h]);
+        tmem_st16(lane_addr + kColO + 16 * i, v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+    };
+
+    if (warp >= 2) {
+      // ---- decode warps: tile t+1 (its buffer was last read by O^T MMA
+      // t-1); warps 2-3 also take lanes 64..127 of an O rescale of tile t
+      if (nt > 0) {
+        wait_bar(smem_u32(&sm.raw_full[0]), 0, abort_flag);
+        decode(0);
+      }
+      int nresc = 0;
+      for (int t = 0; t < nt && !*abort_flag; ++t) {
+        if (t + 1 < nt) {
+          if (t >= 1) wait_bar(smem_u32(&sm.o_done[(t - 1) & 1]), ((t - 1) >> 1) & 1, abort_flag);
+          wait_bar(smem_u32(&sm.raw_full[(t + 1) % kRawStages]), ((t + 1) / kRawStages) & 1,
+                   abort_flag);
+          decode(t + 1);
+        }
+        if (warp < 4) {
+          wait_bar(smem_u32(&sm.p_done[t & 1]), (t >> 1) & 1, abort_flag);
+          if (sm.rescale[t & 1] && !*abort_flag) {
+            rescale_o(t);
+            mbar_arrive(smem_u32(&sm.resc_done));
+            ++nresc;
+          }
+        }
+      }
+    } else {
+      // ---- softmax warps: tile t, one token per thread, all 16 heads
+      int nresc = 0;
+      for (int t = 0; t < nt; ++t) {
+        wait_bar(smem_u32(&sm.s_done[t & 1]), (t >> 1) & 1, abort_flag);
+        tc_fence_after();
+        uint32_t sl[16], sp[16];
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+        tmem_ld16(lane_addr + kColSLat + 16 * (t & 1), sl);
+        tmem_ld16(lane_addr + kColSPe + 16 * (t & 1), sp);
+        tmem_wait_ld();
+        const int r = 32 * warp + lane;
+        const bool valid = r < ntok - t * kT && !*abort_flag;
+        float xs[kMlaHeads];
+        bool need = false;
+#pragma unroll
+        for (int h = 0; h < kMlaHeads; ++h) {
+          xs[h] = valid ? __uint_as_float(sl[h]) * a.qk_scale_log2 +
+                              __uint_as_float(sp[h]) * a.pe_scale_log2
+                        : -INFINITY;
+          need |= xs[h] > m[h] + kLazyMax;
+        }
+        need = __any_sync(0xffffffffu, need);
+        if (lane == 0) sm.need[warp] = need;
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+        const bool any_need = sm.need[0] | sm.need[1];
+        bool resc = false;
+        if (any_need) {
+#pragma unroll
+          for (int h = 0; h < kMlaHeads; ++h) {
+            float mx = xs[h];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (lane == 0) sm.wmax[warp][h] = mx;
+          }
+          asm volatile("bar.sync 1, 64;" ::: "memory");
+#pragma unroll
+          for (int h = 0; h < kMlaHeads; ++h) {
+            const float mx = fmaxf(sm.wmax[0][h], sm.wmax[1][h]);
+            const bool mv = mx > m[h] + kLazyMax;   // also the first finite tile
+            const float alpha = mv ? ex2(m[h] - mx) : 1.f;
+            m[h] = mv ? mx : m[h];
+            l[h] *= alpha;
+            resc |= alpha != 1.f;
+            if (tid == 0) sm.alpha[t & 1][h] = alpha;
+          }
+        }
+        const bool do_resc = any_need && resc && t > 0;   // identical in all 64 threads
+        if (tid == 0) sm.rescale[t & 1] = do_resc ? 1 : 0;
+        const uint32_t pt = base + kOffP + (t & 1) * kPBytes;
+#pragma unroll
+        for (int h = 0; h < kMlaHeads; ++h) {
+          const float pv = ex2(xs[h] - (m[h] == -INFINITY ? 0.f : m[h]));
+          l[h] += pv;
+          sts16(pt + swz(h, r), __half_as_ushort(__float2half_rn(pv)));
+        }
+        fence_proxy_async_shared();
+        tc_fence_before();
+        asm volatile("bar.sync 1, 64;" ::: "memory");   // both warps' P^T and flags written
+        if (tid == 0) mbar_arrive(smem_u32(&sm.p_done[t & 1]));
+        if (do_resc) {
+          rescale_o(t);
+          asm volatile("bar.sync 1, 64;" ::: "memory");
+          if (tid == 0) wait_bar(smem_u32(&sm.resc_done), nresc & 1, abort_flag);
+          ++nresc;
+        }
+        if (tid == 0) mbar_arrive(smem_u32(&sm.p_ready[t & 1]));   // O^T MMA t may go
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+        if (*abort_flag) break;
+      }
+    }
+  }
+  // denominators over the 64 tokens of the softmax warps; the reference max
+  if (warp < 2) {
+#pragma unroll
+    for (int h = 0; h < kMlaHeads; ++h) {
+      float v = l[h];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) sm.lsum[warp][h] = v;
+      if (tid == 0) sm.m[h] = m[h];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const bool bad = *abort_flag != 0;
+  if (bad && tid == 0) record_error(a.error_flag, 1);
+
+  // ---- partials: warp w < 4 holds dims 128 i + 32 w + lane of every block i
+  const size_t part_row = (size_t)b * kMlaHeads;
+  if (warp < 4) {
+    float fac[kMlaHeads];
+#pragma unroll
+    for (int h = 0; h < kMlaHeads; ++h) {
+      const float lt = sm.lsum[0][h] + sm.lsum[1][h];
+      fac[h] = lt > 0.f ? __fdividef(a.out_mult, lt) : 0.f;
+    }
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+#pragma unroll 1
+    for (int i = 0; i < kMlaLat / 128; ++i) {
+      uint32_t v[16];
+      if (nt > 0 && !bad) {
+        tmem_ld16(lane_addr + kColO + 16 * i, v);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int h = 0; h < kMlaHeads; ++h) v[h] = 0u;
+      }
+      float* po = a.part_o + (part_row * a.num_splits + split) * kMlaLat + 128 * i + 32 * warp + lane;
+#pragma unroll
+      for (int h = 0; h < kMlaHeads; ++h)
+        po[(size_t)h * a.num_splits * kMlaLat] = bad ? NAN : __uint_as_float(v[h]) * fac[h];
+    }
+  }
+  if (tid < kMlaHeads) {
+    const float lt = sm.lsum[0][tid] + sm.lsum[1][tid];
+    const float mm = sm.m[tid];
+    a.part_lse[(part_row + tid) * a.num_splits + split] =
+        bad ? NAN : (mm == -INFINITY || lt == 0.f) ? -INFINITY : (mm + log2f(lt)) * kLn2;
+  }
+  // ---- tensor memory back; then the fused combine
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+  if (a.counters) mla_fused_combine(a, b, part_row, base, gbase, smem_u32(&sm.comb_full));
+}
 }  // namespace
 
-cudaError_t launch_mla_partial(const CUtensorMap& tkv, const CUtensorMap& tpe,
+cudaError_t launch_mla_partial(const CUtensorMap& tcodes, const CUtensorMap& tpe,
+                               const CUtensorMap& tcodes64, const CUtensorMap& tpe64,
                                const PartialArgs& a, cudaStream_t st) {
-  static_assert(kMlaHeads * kMlaLat * 4 <= kMlaRing, "the output buffer must fit in the ring");
-  cudaError_t e = cudaFuncSetAttribute(mla_partial_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmem);
+  cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(mla_partial_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           (int)cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(mla_partial_kernel, dim3(a.batch, a.num_splits), dim3(kDecodeThreads),
-                    (size_t)kMlaSmem, st, tkv, tpe, a);
+  return launch_pdl(mla_tc_kernel, dim3(a.batch, a.num_splits), dim3(kThreads),
+                    (size_t)kSmemBytes, st, tcodes, tpe, tcodes64, tpe64, a);
 }
 
 }  // namespace kvq

@@ -74,10 +74,12 @@ def test_auto_splits():
     assert f(152, 64, 16, 1, 2048, 1) == (0, 1)
     assert f(152, 64, 16, 1, 2049, 1) == (0, 2)
     assert f(152, 4, 8, 4, 200000, 1) == (0, 64)
-    # MLA (16 heads on one kv head: two CTAs per SM): floor(304 / 32) = 9
-    assert f(152, 32, 1, 16, 4096, 2) == (0, 9)
-    assert f(152, 2, 1, 12, 32768, 1) == (0, 64)
+    # MLA shape (NVFP4, 16 heads on one kv head: one CTA per SM): floor(152 / 32) = 4
+    assert f(152, 32, 1, 16, 4096, 2) == (0, 4)
     assert f(152, 128, 1, 16, 4096, 2) == (0, 2)
+    # 16 FP8 heads on one kv head: two CTAs per SM, floor(304 / 32) = 9
+    assert f(152, 32, 1, 16, 4096, 1) == (0, 9)
+    assert f(152, 2, 1, 12, 32768, 1) == (0, 64)
     # clamp at 64
     assert f(152, 1, 1, 4, 1 << 20, 2) == (0, 64)
     assert f(0, 1, 1, 1, 10, 1)[0] == kvq.KVQ_ERR_INVALID
