@@ -15,7 +15,10 @@ on the launch stream (the two launches are replayed as one CUDA graph).
 `value` is the mean device time per step in microseconds (lower is better); KV GB/s = attended cache bytes / step time.
 
     python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
-                    [--no-sweep]
+                    [--no-sweep] [--workload gqa_fp8|nvfp4|paged_fp8_probs|mla_nvfp4]
+
+--workload picks the workload of the main line (default: the headline GQA
+FP8 workload above); the others are the sweep's workloads at their own sizes.
 
 With --impl reference the CPU oracle is timed on the same workload on the
 host cores (the reference arm); under torchrun only rank 0 runs it.
@@ -62,23 +65,29 @@ def hbm_peak():
         return 6800.0, "fallback"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {
+    "decode": ["kvq_decode.cu", "kvq_attn.cuh", "kvq_device.cuh", "kvq_internal.h"],
+    "mla": ["kvq_mla.cu", "kvq_attn.cuh", "kvq_device.cuh", "kvq_internal.h"],
+}
+
+
+def kernel_source_hash(kind: str = "decode"):
     h = hashlib.sha256()
-    for f in ["kvq_decode.cu", "kvq_attn.cuh", "kvq_device.cuh", "kvq_internal.h"]:
+    for f in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, "quantized_kv_cache_05_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes per launch of the partial kernel from the committed ncu
+def ncu_traffic(workload: str, kind: str = "decode"):
+    """DRAM bytes per launch of the decode kernel from the committed ncu
     summary, when it was taken on the current kernel source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
         e = d.get(workload)
-        if e and e.get("source_hash") == kernel_source_hash():
+        if e and e.get("source_hash") == kernel_source_hash(kind):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -339,6 +348,43 @@ class Bench:
         return self.kv_bytes() + bt + q + parts + out
 
 
+def _workloads():
+    from quantized_kv_cache_05_gb300 import synth
+    return {
+        "gqa_fp8": {
+            "make": lambda L: synth.gqa_fp8(L), "kind": "decode",
+            "kernel": "partial_kernel<FP8,128> (kvq_decode, fused combine)",
+            "dtype": "fp8_e4m3 KV codes -> f16 mma.sync, f32 accumulate",
+            "data": "synthetic (seeded bf16 N(0,1), 1% x10 outliers)",
+            "desc": lambda w: (f"gqa_fp8: batch {w.B}, Hq {w.Hq}, Hkv {w.Hkv}, head_dim {w.D}, "
+                               f"kv_len {int(w.Lmax)}, FP8 E4M3 per-tensor KV, bf16 out, s=auto")},
+        "nvfp4": {
+            "make": lambda L: synth.nvfp4(L), "kind": "decode",
+            "kernel": "partial_kernel<NVFP4,128> (kvq_decode, fused combine)",
+            "dtype": "nvfp4 (e2m1 + e4m3 block scales) KV -> f16 mma.sync, f32 accumulate",
+            "data": "synthetic (seeded bf16 N(0,1))",
+            "desc": lambda w: (f"nvfp4: batch {w.B}, Hq {w.Hq}, Hkv {w.Hkv}, head_dim {w.D}, "
+                               f"kv_len {int(w.Lmax)}, NVFP4 KV, f32 out, s=auto")},
+        "paged_fp8_probs": {
+            "make": lambda L: synth.paged_fp8_probs(), "kind": "decode",
+            "kernel": "partial_kernel<FP8,128,probq> (kvq_decode, fused combine)",
+            "dtype": "fp8_e4m3 KV and probabilities -> f16 mma.sync, f32 accumulate",
+            "data": "synthetic (seeded bf16 N(0,1); lengths uniform 512..8192)",
+            "desc": lambda w: (f"paged_fp8_probs: batch {w.B}, MHA {w.Hq} heads, head_dim {w.D}, "
+                               f"16-token pages in random order, FP8 probabilities, E4M3 out, s=auto")},
+        "mla_nvfp4": {
+            "make": lambda L: synth.mla_nvfp4(), "kind": "mla",
+            "kernel": "mla_tc_kernel (tcgen05, kvq_decode with fused combine)",
+            "dtype": "nvfp4 latent -> f16 tcgen05.mma, bf16 rope, f32 accumulate in TMEM",
+            "data": "synthetic (seeded bf16 N(0,1))",
+            "desc": lambda w: (f"mla_nvfp4: batch {w.B}, 16 heads, NVFP4 latent 512 + bf16 rope 64, "
+                               f"kv_len {int(w.Lmax)}, f32 out, s=auto")},
+    }
+
+
+WORKLOADS = None
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -349,7 +395,8 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     device = torch.device("cuda", local)
-    w = synth.gqa_fp8(args.kv_len)
+    spec = WORKLOADS[args.workload]
+    w = spec["make"](args.kv_len)
     bench = Bench(w, device)
     peak, peak_kind = hbm_peak()
 
@@ -367,7 +414,7 @@ def run_ours(args):
     e2e_us, bi, bo = bench.e2e(max(10, args.steps // 2), args.warmup)
     part = statistics.mean(part_us)
     achieved = bench.partial_bytes() / (part * 1e-6) / 1e9
-    traffic = ncu_traffic(f"gqa_fp8_L{args.kv_len}")
+    traffic = ncu_traffic(w.name, spec["kind"])
     kvb = bench.kv_bytes()
     line = {
         "metric": METRIC,
@@ -380,12 +427,11 @@ def run_ours(args):
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8_e4m3 KV codes -> f16 mma.sync, f32 accumulate",
-        "data": "synthetic (seeded bf16 N(0,1), 1% x10 outliers)",
+        "dtype": spec["dtype"],
+        "data": spec["data"],
         "config": {
-            "workload": f"gqa_fp8: batch 2, Hq 32, Hkv 8, head_dim 128, kv_len {args.kv_len}, "
-                        f"FP8 E4M3 per-tensor KV, bf16 out, s=auto",
-            "batch": w.B, "kv_len": args.kv_len, "splits": bench.splits,
+            "workload": spec["desc"](w),
+            "batch": w.B, "kv_len": int(w.Lmax), "splits": bench.splits,
             "step": "append 1 token + kvq_decode (partial with fused combine, overlapping the append: fresh_tokens=1), one CUDA graph",
             "l2": "flushed before every timed step (256 MiB write, then 256 MiB read)",
             "parallelism": "replicas" if world > 1 else "single GPU",
@@ -395,7 +441,7 @@ def run_ours(args):
         "kv_hbm_frac": round(kvb / (us * 1e-6) / 1e9 / peak, 4),
         "partial_us": round(part, 3),
         "roofline": {
-            "kernel": "partial_kernel<FP8,128> (kvq_decode, fused combine)",
+            "kernel": spec["kernel"],
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -567,7 +613,11 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sweep-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload", default="gqa_fp8",
+                    choices=["gqa_fp8", "nvfp4", "paged_fp8_probs", "mla_nvfp4"])
     args = ap.parse_args()
+    global WORKLOADS
+    WORKLOADS = _workloads()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -191,15 +191,6 @@ __device__ __forceinline__ void store_out_t(void* out, float out_scale, size_t i
   }
 }
 
-__device__ __forceinline__ void store_out(void* out, int dtype, float out_scale, size_t i, float v) {
-  if (dtype == 0) {
-    static_cast<float*>(out)[i] = v;
-  } else if (dtype == 1) {
-    static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
-  } else {
-    static_cast<uint8_t*>(out)[i] = (uint8_t)(f32x2_to_e4m3x2(__fdiv_rn(v, out_scale), 0.f) & 0xFFu);
-  }
-}
 
 // Merge of the s split partials of `rows` consecutive query heads starting at
 // partial row `row0` (M = max lse, w_j = e^(lse_j - M), O = sum w_j o_j /
@@ -334,19 +325,48 @@ __device__ __forceinline__ void merge_rows(const float* __restrict__ part_o,
                            out_scale);
 }
 
-// Fused combine: the last CTA of a (request, kv head) to finish merges the
-// s partials of its G query heads and writes the output; it then resets the
-// arrival counter for the next call.  The arrival is one acq_rel atomic by
-// thread 0 after a CTA barrier: its release orders the CTA's partial stores
-// (made before the barrier) before the arrival, and in the last CTA its
-// acquire, extended to the CTA by the second barrier, makes every other
-// CTA's partials visible.  wbuf: kMaxGroup * (kMaxFusedSplits + 1) floats of
-// shared memory.  DEPTH: loads in flight per thread (register budget); NI:
-// float4 columns per thread and round (several when a thread owns many
-// columns and s is small).
+// Staged merge: the s partials of rows [row0, row0 + rows) are contiguous in
+// global memory ([row][split][Dv] floats); with them in shared memory (one
+// bulk copy) the weighted sum is a short loop, four value dims per thread and
+// step.
+template <int DT>
+__device__ __forceinline__ void merge_staged(const PartialArgs& a, size_t row0, int rows,
+                                             const float* staged, const float* w,
+                                             const float* winv, bool ok) {
+  const int s = a.num_splits, nq = a.Dv / 4;
+  const float4* po = reinterpret_cast<const float4*>(staged);
+#pragma unroll 1
+  for (int i = threadIdx.x; i < rows * nq; i += blockDim.x) {
+    const int r = i / nq, d4 = i % nq;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int j = 0; j < s; ++j) {
+      const float wj = w[r * kMaxFusedSplits + j];
+      const float4 v = po[(r * s + j) * nq + d4];
+      acc.x += wj * v.x;
+      acc.y += wj * v.y;
+      acc.z += wj * v.z;
+      acc.w += wj * v.w;
+    }
+    const float iv = ok ? winv[r] : NAN;
+    const size_t o = (row0 + r) * a.Dv + 4 * d4;
+    store_out_t<DT>(a.out, a.out_scale, o + 0, acc.x * iv);
+    store_out_t<DT>(a.out, a.out_scale, o + 1, acc.y * iv);
+    store_out_t<DT>(a.out, a.out_scale, o + 2, acc.z * iv);
+    store_out_t<DT>(a.out, a.out_scale, o + 3, acc.w * iv);
+  }
+}
+
+// Fused combine with staging: the arrival protocol of fused_combine; the
+// last CTA brings its rows' partials into shared memory with one bulk copy
+// when they fit in `cap` bytes at `stage` (16-byte aligned, free), else it
+// runs the general merge.  The async-proxy read follows the acquire, behind
+// a proxy fence.  bar: an mbarrier initialized with one arrival and unused
+// so far; wbuf: kMaxGroup * (kMaxFusedSplits + 1) floats outside the stage.
 template <int DEPTH = 32, int NI = 1>
-__device__ __forceinline__ void fused_combine(const PartialArgs& a, int bh, size_t part_row,
-                                              float* wbuf) {
+__device__ __forceinline__ void fused_combine_staged(const PartialArgs& a, int bh, size_t part_row,
+                                                     int rows, uint32_t stage, const float* stage_p,
+                                                     uint32_t cap, float* wbuf, uint32_t bar) {
   __shared__ int is_last;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -360,8 +380,29 @@ __device__ __forceinline__ void fused_combine(const PartialArgs& a, int bh, size
   }
   __syncthreads();
   if (!is_last) return;
-  merge_rows_t<NI, DEPTH / NI>(a.part_o, a.part_lse, part_row, a.G, a.num_splits, a.Dv, wbuf,
-             wbuf + kMaxGroup * kMaxFusedSplits, a.out, a.out_dtype, a.out_scale);
+  const int s = a.num_splits;
+  float* winv = wbuf + kMaxGroup * kMaxFusedSplits;
+  const uint64_t bytes = (uint64_t)rows * s * a.Dv * 4;
+  if (bytes > cap) {
+    merge_rows_t<NI, DEPTH / NI>(a.part_o, a.part_lse, part_row, rows, s, a.Dv, wbuf, winv,
+                                 a.out, a.out_dtype, a.out_scale);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");   // acquired data -> bulk copy
+    mbar_arrive_expect_tx(bar, (uint32_t)bytes);
+    bulk_load(stage, a.part_o + part_row * s * a.Dv, (uint32_t)bytes, bar);
+  }
+  merge_weights(a.part_lse, part_row, rows, s, wbuf, winv);
+  const bool ok = mbar_wait(bar, 0);
+  __syncthreads();
+  if (a.out_dtype == 0)
+    merge_staged<0>(a, part_row, rows, stage_p, wbuf, winv, ok);
+  else if (a.out_dtype == 1)
+    merge_staged<1>(a, part_row, rows, stage_p, wbuf, winv, ok);
+  else
+    merge_staged<2>(a, part_row, rows, stage_p, wbuf, winv, ok);
+  if (!ok && threadIdx.x == 0) record_error(a.error_flag, 1);
 }
 
 }  // namespace kvq

@@ -48,6 +48,7 @@ namespace {
 
 struct Smem {
   uint64_t full[kDecodeWarps][kStages];
+  uint64_t comb_full;   // fused combine: partials landed
   int abort_flag;
   int pages[kPageCache];
   float m[kDecodeWarps][kMaxGroup];
@@ -109,6 +110,7 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, PROBQ, NH>())
   if (threadIdx.x == 0) sm.abort_flag = 0;
   if (lane == 0) {
     for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&sm.full[warp][i]), 1);
+    if (warp == 0) mbar_init(smem_u32(&sm.comb_full), 1);
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -512,9 +514,15 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, PROBQ, NH>())
     if (h0 + 1 < a.G) *reinterpret_cast<float2*>(r0 + (size_t)a.num_splits * D) =
         make_float2(acc.y, acc.w);
   }
-  if (a.counters)
-    fused_combine<ctas_per_sm<FMT, PROBQ, NH>() == 4 ? 16 : 32>(a, bh, part_row,
-                  reinterpret_cast<float*>(ofrag + kDecodeWarps * MT * NH * 32));
+  // fused combine: the G rows' partials staged at the ring base (the O
+  // fragments are written out), the weights at the ring end
+  if (a.counters) {
+    constexpr uint32_t kWbuf = (kMaxGroup * kMaxFusedSplits + kMaxGroup) * 4;
+    fused_combine_staged<ctas_per_sm<FMT, PROBQ, NH>() == 4 ? 16 : 32>(
+        a, bh, part_row, a.G, ring, reinterpret_cast<const float*>(ofrag), Rg::kBytes - kWbuf,
+        reinterpret_cast<float*>(dyn_smem + (ring - smem_u32(dyn_smem)) + Rg::kBytes - kWbuf),
+        smem_u32(&sm.comb_full));
+  }
 }
 
 // ---------------------------------------------------------------------------

@@ -202,82 +202,6 @@ __device__ __forceinline__ void wait_bar(uint32_t bar, uint32_t parity, volatile
   if (!mbar_wait(bar, parity)) *abort_flag = 1;
 }
 
-// Weighted sum of the s staged partials [16][s][512] (shared memory) into
-// the output, four value dims per thread and step.
-template <int DT>
-__device__ __forceinline__ void mla_merge_smem(const PartialArgs& a, size_t part_row, int s,
-                                               const uint8_t* staged, const float* w,
-                                               const float* winv, bool ok) {
-  const float4* po = reinterpret_cast<const float4*>(staged);
-  constexpr int nq = kMlaLat / 4;
-#pragma unroll 1
-  for (int i = threadIdx.x; i < kMlaHeads * nq; i += blockDim.x) {
-    const int r = i / nq, d4 = i % nq;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-    for (int j = 0; j < s; ++j) {
-      const float wj = w[r * kMaxFusedSplits + j];
-      const float4 v = po[(r * s + j) * nq + d4];
-      acc.x += wj * v.x;
-      acc.y += wj * v.y;
-      acc.z += wj * v.z;
-      acc.w += wj * v.w;
-    }
-    const float iv = ok ? winv[r] : NAN;
-    const size_t o = (part_row + r) * kMlaLat + 4 * d4;
-    store_out_t<DT>(a.out, a.out_scale, o + 0, acc.x * iv);
-    store_out_t<DT>(a.out, a.out_scale, o + 1, acc.y * iv);
-    store_out_t<DT>(a.out, a.out_scale, o + 2, acc.z * iv);
-    store_out_t<DT>(a.out, a.out_scale, o + 3, acc.w * iv);
-  }
-}
-
-// Fused combine of the MLA kernel: the last CTA of a request merges the s
-// partials of its 16 heads.  With s <= 4 the partials (16 x s x 512 floats,
-// contiguous) come into shared memory with one bulk copy and are summed by a
-// short loop; otherwise the general merge runs.  The arrival protocol is the
-// GQA kernel's (one acq_rel atomic after a CTA barrier).
-__device__ __forceinline__ void mla_fused_combine(const PartialArgs& a, int b, size_t part_row,
-                                                  uint32_t base, uint8_t* gbase, uint32_t bar) {
-  __shared__ int is_last;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    unsigned prev;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                 : "=r"(prev)
-                 : "l"(a.counters + b)
-                 : "memory");
-    is_last = prev == (unsigned)(a.num_splits - 1);
-    if (is_last) a.counters[b] = 0u;
-  }
-  __syncthreads();
-  if (!is_last) return;
-  const int s = a.num_splits;
-  float* wbuf = reinterpret_cast<float*>(gbase + kOffRaw);
-  float* winv = wbuf + kMaxGroup * kMaxFusedSplits;
-  if (s > 4) {
-    merge_rows_t<4, 8>(a.part_o, a.part_lse, part_row, kMlaHeads, s, kMlaLat, wbuf, winv, a.out,
-                       a.out_dtype, a.out_scale);
-    return;
-  }
-  const uint32_t bytes = (uint32_t)(kMlaHeads * s * kMlaLat * 4);   // <= 128 KB: the two tiles
-  if (threadIdx.x == 0) {
-    asm volatile("fence.proxy.async.global;" ::: "memory");   // acquired data -> bulk copy
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_load(base + kOffTile, a.part_o + part_row * s * kMlaLat, bytes, bar);
-  }
-  merge_weights(a.part_lse, part_row, kMlaHeads, s, wbuf, winv);
-  const bool ok = mbar_wait(bar, 0);
-  __syncthreads();
-  if (a.out_dtype == 0)          // fp32
-    mla_merge_smem<0>(a, part_row, s, gbase + kOffTile, wbuf, winv, ok);
-  else if (a.out_dtype == 1)     // bf16
-    mla_merge_smem<1>(a, part_row, s, gbase + kOffTile, wbuf, winv, ok);
-  else
-    mla_merge_smem<2>(a, part_row, s, gbase + kOffTile, wbuf, winv, ok);
-  if (!ok && threadIdx.x == 0) record_error(a.error_flag, 1);
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     mla_tc_kernel(const __grid_constant__ CUtensorMap tmCodes,
                   const __grid_constant__ CUtensorMap tmPe,
@@ -740,7 +664,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                  "r"(kTmemCols)
                  : "memory");
   }
-  if (a.counters) mla_fused_combine(a, b, part_row, base, gbase, smem_u32(&sm.comb_full));
+  // fused combine: the partials of the request (16 x s x 512 floats) staged
+  // in the two tile buffers (128 KB), the weights in the raw ring
+  if (a.counters)
+    fused_combine_staged<32, 4>(a, b, part_row, kMlaHeads, base + kOffTile,
+                                reinterpret_cast<const float*>(gbase + kOffTile), 2 * kTileBytes,
+                                reinterpret_cast<float*>(gbase + kOffRaw), smem_u32(&sm.comb_full));
 }
 }  // namespace
 
