@@ -220,6 +220,9 @@ class Bench:
             self.start_pos = torch.tensor(last, dtype=torch.int32, device=device)
             self.seq_lens = torch.from_numpy(np.ascontiguousarray(w.seq_lens, np.int32)).to(device)
             del dev_rows, kpe_rows
+            # the step's inputs (q and the new K/V rows) as views of one device
+            # buffer, so that the end-to-end step moves them with one copy
+            self._pack_inputs()
         self.stream.synchronize()
         self.splits = splits or runtime.auto_splits(B, Hkv, w.G, w.Lmax, w.fmt, device)
         self.out_scale = 1.0
@@ -239,6 +242,25 @@ class Bench:
         self.graph_step = self._capture(full=True)
         self.graph_partial = self._capture(full=False)
 
+    def _pack_inputs(self):
+        t = self.torch
+        parts = [x for x in (self.q, self.k_new, self.v_new, self.kpe_new) if x is not None]
+        offs, n = [], 0
+        for x in parts:
+            offs.append(n)
+            n += (x.numel() * x.element_size() + 255) // 256 * 256
+        self.inputs = t.empty(n, dtype=t.uint8, device=self.device)
+        views = []
+        for x, o in zip(parts, offs):
+            v = self.inputs[o:o + x.numel() * x.element_size()].view(x.dtype).view(x.shape)
+            v.copy_(x)
+            views.append(v)
+        it = iter(views)
+        self.q = next(it)
+        self.k_new = next(it)
+        self.v_new = next(it) if self.v_new is not None else None
+        self.kpe_new = next(it) if self.kpe_new is not None else None
+
     def _bf16(self, a):
         t = self.torch
         a = np.ascontiguousarray(a, np.uint16)
@@ -249,17 +271,19 @@ class Bench:
         return self.runtime.DecodeConfig(w.B, w.Hq, w.Dqk, w.Dv, getattr(self, "splits", 1),
                                          w.Lmax, w.sm_scale, w.prob_scale, out, out_scale)
 
-    def _launch(self, full: bool, stream):
-        """full: append + kvq_decode (one step); else kvq_decode alone."""
+    def _launch(self, full: bool, stream, io=None):
+        """full: append + kvq_decode (one step); else kvq_decode alone.  io:
+        (q, k_new, v_new, kpe_new, out) to use instead of the device tensors
+        (e.g. pinned host memory)."""
         kvq = self.kvq
         c = self.cache.struct()
         p = self.cfg.params(self.seq_lens)
+        q, k, v, kpe, out = io or (self.q, self.k_new, self.v_new, self.kpe_new, self.ws.out)
         if full:
-            kvq.check(kvq.kvq_quantize_append(c, self.k_new, self.v_new, self.kpe_new,
-                                              self.start_pos, self.w.B, 1, stream))
+            kvq.check(kvq.kvq_quantize_append(c, k, v, kpe, self.start_pos, self.w.B, 1, stream))
             p.fresh_tokens = 1   # the decode overlaps with the append of the last position
-        kvq.check(kvq.kvq_decode(c, p, self.q, self.ws.part_o, self.ws.part_lse, self.ws.counters,
-                                 self.ws.out, stream))
+        kvq.check(kvq.kvq_decode(c, p, q, self.ws.part_o, self.ws.part_lse, self.ws.counters,
+                                 out, stream))
 
     def _capture(self, full: bool):
         t = self.torch
@@ -295,13 +319,13 @@ class Bench:
         return [a.elapsed_time(b) * 1e3 for a, b in times]   # microseconds
 
     def e2e(self, steps: int, warmup: int):
-        """Through the public API with host buffers: pinned H2D of the step's
-        q and new K/V rows, append + partial + combine, D2H of the output."""
+        """Through the public API with host buffers: one pinned H2D copy of the
+        step's q and new K/V rows (packed), append + kvq_decode, D2H of the
+        output."""
         t = self.torch
-        pin = lambda x: x.cpu().pin_memory() if x is not None else None
-        hq, hk, hv, hkpe = pin(self.q), pin(self.k_new), pin(self.v_new), pin(self.kpe_new)
+        hin = self.inputs.cpu().pin_memory()   # q and the new K/V rows, packed
         hout = t.empty(self.ws.out.shape, dtype=self.ws.out.dtype).pin_memory()
-        bi = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hkpe) if x is not None)
+        bi = hin.numel()
         bo = hout.numel() * hout.element_size()
         times = []
         with t.cuda.stream(self.stream):
@@ -310,12 +334,7 @@ class Bench:
                 e0 = t.cuda.Event(enable_timing=True)
                 e1 = t.cuda.Event(enable_timing=True)
                 e0.record(self.stream)
-                self.q.copy_(hq, non_blocking=True)
-                self.k_new.copy_(hk, non_blocking=True)
-                if hv is not None:
-                    self.v_new.copy_(hv, non_blocking=True)
-                if hkpe is not None:
-                    self.kpe_new.copy_(hkpe, non_blocking=True)
+                self.inputs.copy_(hin, non_blocking=True)
                 self._launch(True, self.stream)
                 hout.copy_(self.ws.out, non_blocking=True)
                 e1.record(self.stream)
@@ -323,6 +342,36 @@ class Bench:
                 if i >= warmup:
                     times.append(e0.elapsed_time(e1) * 1e3)
         return statistics.mean(times), bi, bo
+
+    def e2e_zero_copy(self, steps: int, warmup: int):
+        """Through the public API with host buffers read and written in place:
+        q and the new K/V rows in pinned host memory (packed), the output too;
+        the kernels reach them over the CPU-GPU link (no separate copies)."""
+        t = self.torch
+        hin = self.inputs.cpu().pin_memory()
+        hout = t.empty(self.ws.out.shape, dtype=self.ws.out.dtype).pin_memory()
+        views, off = [], 0
+        for x in (self.q, self.k_new, self.v_new, self.kpe_new):
+            if x is None:
+                views.append(None)
+                continue
+            o = x.data_ptr() - self.inputs.data_ptr()
+            views.append(hin[o:o + x.numel() * x.element_size()].view(x.dtype).view(x.shape))
+        io = (views[0], views[1], views[2], views[3], hout)
+        times = []
+        with t.cuda.stream(self.stream):
+            for i in range(warmup + steps):
+                self.flush_l2(i)
+                e0 = t.cuda.Event(enable_timing=True)
+                e1 = t.cuda.Event(enable_timing=True)
+                e0.record(self.stream)
+                self._launch(True, self.stream, io)
+                e1.record(self.stream)
+                e1.synchronize()
+                if i >= warmup:
+                    times.append(e0.elapsed_time(e1) * 1e3)
+        same = bool(t.equal(hout, self.ws.out.cpu()))
+        return statistics.mean(times), hin.numel(), hout.numel() * hout.element_size(), same
 
     def kv_bytes(self) -> int:
         """Attended cache bytes per step: codes (+ block scales, + rope keys)."""
@@ -412,6 +461,7 @@ def run_ours(args):
         dist.barrier()
     us = max_over_ranks(statistics.mean(step_us), device)
     e2e_us, bi, bo = bench.e2e(max(10, args.steps // 2), args.warmup)
+    zc_us, zbi, zbo, zc_same = bench.e2e_zero_copy(max(10, args.steps // 2), args.warmup)
     part = statistics.mean(part_us)
     achieved = bench.partial_bytes() / (part * 1e-6) / 1e9
     traffic = ncu_traffic(w.name, spec["kind"])
@@ -452,7 +502,12 @@ def run_ours(args):
             "traffic": traffic,
         },
         "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": bi,
-                "d2h_bytes_per_step": bo},
+                "d2h_bytes_per_step": bo,
+                "method": "one pinned H2D copy of q + new K/V rows, append + kvq_decode, one D2H copy"},
+        "e2e_zero_copy": {"value": round(zc_us, 3), "unit": "us/step", "h2d_bytes_per_step": zbi,
+                          "d2h_bytes_per_step": zbo, "output_matches_device_run": zc_same,
+                          "method": "kernels read q + new K/V rows from pinned host memory and "
+                                    "write the output there (NVLink-C2C), no separate copies"},
         "gpu_launches": 2 * args.steps + args.steps,
         "clocks": clk.summary(),
     }

@@ -25,7 +25,12 @@
  *    and owned by the caller.  The library allocates no memory and keeps no
  *    per-call state; calls are re-entrant.
  *  - Pointers marked (device) must be device (or managed) memory of the
- *    current CUDA device; pointers marked (host) are read on the host.
+ *    current CUDA device; pointers marked (host) are read on the host.  The
+ *    per-step inputs read with plain loads -- q, k_new, v_new, kpe_new --
+ *    and the decode output may also be pinned host memory (page-locked and
+ *    mapped, as cudaHostAlloc gives): the kernels then read and write it in
+ *    place over the CPU-GPU link.  The cache, block table, seq_lens and the
+ *    scratch must be device memory (the cache is read by TMA).
  *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *    NULL = the legacy default stream).  No call synchronizes.
  *  - Every call validates its arguments first and returns KVQ_ERR_INVALID or
