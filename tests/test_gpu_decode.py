@@ -231,6 +231,25 @@ def test_fused_vs_oracle_all_formats(tiny, nv, paged):
         assert_e4m3_close(out.cpu().numpy(), ref, out_scale, f"fused paged e4m3 s={s}")
 
 
+@pytest.fixture(scope="module")
+def gqa4k():
+    S = Setup(synth.gqa_fp8(4096))
+    return S, S.oracle_decode()[0]
+
+
+@pytest.mark.parametrize("s", [29, 30, 40, 64])
+def test_fused_many_splits(gqa4k, s):
+    """Up to 29 splits the last CTA stages the partials of its 4 heads (61 KB)
+    in shared memory; beyond that it merges from global memory.  Both paths
+    give the two-launch result (fp32 sums in the same split order)."""
+    S, ref = gqa4k
+    a, _ = S.gpu_decode(s)
+    b, ws = fused(S, s)
+    assert_f32_close(b.cpu().numpy(), ref, f"fused s={s}")
+    assert torch.allclose(a, b, rtol=4e-7, atol=1e-7)
+    assert not ws.counters.any()
+
+
 def test_fused_workspace_reuse_across_split_counts(gqa):
     """One scratch set (sized for 8 splits) serves calls with fewer splits.
     The fused merge sums the split weights sequentially and the combine
@@ -260,7 +279,7 @@ def test_mla_two_launch(mla, s):
     assert_f32_close(out.cpu().numpy(), ref, f"mla s={s}")
 
 
-@pytest.mark.parametrize("s", [1, 4])
+@pytest.mark.parametrize("s", [1, 4, 5, 9])   # s > 4: the merge reads global memory
 def test_mla_fused(mla, s):
     ref, _ = mla.oracle_decode()
     out, ws = fused(mla, s)
