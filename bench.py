@@ -72,10 +72,16 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_hash(kind: str = "decode"):
+    """Hash of the kernel sources with comments and whitespace removed (the
+    counters of a capture depend on the code only)."""
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kind]:
-        with open(os.path.join(ROOT, "quantized_kv_cache_05_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "quantized_kv_cache_05_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -7,7 +7,8 @@
 // s partials.  FP8 probabilities and FP8 output follow vLLM PR 15734.
 //
 // GB300 design of the partial kernel
-//  * Four warps per CTA, three CTAs per SM.  Each warp streams its own
+//  * Four warps per CTA, three CTAs per SM (four in the FP8-probability
+//    mode, whose ring holds one tensor per stage).  Each warp streams its own
 //    16-token boxes (box w, w+4, w+8, ... of the chunk) HBM -> shared memory
 //    with TMA (cp.async.bulk.tensor, 16-row box = one 16-token page,
 //    hardware swizzle; NVFP4 block scales by 1-D bulk copies) into a private
@@ -34,7 +35,9 @@
 //  * The running max moves only when a box's max exceeds it by more than
 //    2^8 (log2 domain), so O is rarely rescaled; the final normalization by
 //    the denominator is exact whatever the reference max.
-//  * Warps merge their (max, sum, O) states through shared memory at the end.
+//  * Warps merge their (max, sum, O) states through shared memory at the end
+//    (O in MMA-fragment order); the last CTA of a (request, kv head) merges
+//    the split partials in the same launch when the arrival counters are given.
 // Every mbarrier wait is bounded; a timeout sets an error bit and the CTA
 // writes NaN for its partial instead of hanging.
 
