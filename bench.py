@@ -324,6 +324,23 @@ class Bench:
         self.stream.synchronize()
         return [a.elapsed_time(b) * 1e3 for a, b in times]   # microseconds
 
+    def time_plain(self, full: bool, steps: int, warmup: int):
+        """The same step launched directly through the API (no CUDA graph)."""
+        t = self.torch
+        times = []
+        with t.cuda.stream(self.stream):
+            for i in range(warmup + steps):
+                self.flush_l2(i)
+                e0 = t.cuda.Event(enable_timing=True)
+                e1 = t.cuda.Event(enable_timing=True)
+                e0.record(self.stream)
+                self._launch(full, self.stream)
+                e1.record(self.stream)
+                if i >= warmup:
+                    times.append((e0, e1))
+        self.stream.synchronize()
+        return [a.elapsed_time(b) * 1e3 for a, b in times]
+
     def e2e(self, steps: int, warmup: int):
         """Through the public API with host buffers: one pinned H2D copy of the
         step's q and new K/V rows (packed), append + kvq_decode, D2H of the
@@ -462,6 +479,7 @@ def run_ours(args):
     with ClockSampler(local) as clk:
         step_us = bench.time_graph(bench.graph_step, args.steps, args.warmup)
         part_us = bench.time_graph(bench.graph_partial, args.steps, args.warmup)
+        plain_us = bench.time_plain(True, args.steps, args.warmup)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -495,6 +513,8 @@ def run_ours(args):
         "kv_bytes_per_step": kvb,
         "kv_gbs": round(kvb / (us * 1e-6) / 1e9, 1),
         "kv_hbm_frac": round(kvb / (us * 1e-6) / 1e9 / peak, 4),
+        "step_stats_us": pct(step_us),
+        "plain_launch_us": pct(plain_us),
         "partial_us": round(part, 3),
         "roofline": {
             "kernel": spec["kernel"],
@@ -514,7 +534,8 @@ def run_ours(args):
                           "d2h_bytes_per_step": zbo, "output_matches_device_run": zc_same,
                           "method": "kernels read q + new K/V rows from pinned host memory and "
                                     "write the output there (NVLink-C2C), no separate copies"},
-        "gpu_launches": 2 * args.steps + args.steps,
+        # graph step (append + decode), graph partial (decode), plain step
+        "gpu_launches": 2 * args.steps + args.steps + 2 * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_sweep:
@@ -526,6 +547,14 @@ def run_ours(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def pct(xs):
+    """mean, median, p10 and p90 of per-step times (microseconds)."""
+    a = np.asarray(xs, dtype=np.float64)
+    return {"mean": round(float(a.mean()), 3), "median": round(float(np.median(a)), 3),
+            "p10": round(float(np.percentile(a, 10)), 3),
+            "p90": round(float(np.percentile(a, 90)), 3), "n": int(a.size)}
 
 
 def sweep(device, args):
@@ -666,8 +695,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--kv-len", type=int, default=HEADLINE_L)
     ap.add_argument("--no-sweep", action="store_true")

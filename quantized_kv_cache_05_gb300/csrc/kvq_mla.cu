@@ -15,7 +15,7 @@
 // warp-specialized roles that hand work over through mbarriers:
 //  * a TMA warp streams each tile's latent codes (128-byte swizzled boxes),
 //    block scales (1-D bulk copy) and rope keys into a two-stage ring;
-//  * six decode warps turn a tile, once, into an f16 [token][dim] tile
+//  * eight decode warps turn a tile, once, into an f16 [token][dim] tile
 //    (E2M1 x E4M3 -> f16 is exact) in the 128-byte-swizzled layout that is
 //    the K-major A operand of S^T = K Q^T and, read MN-major, the A operand
 //    of O^T = V^T P^T; they copy the rope keys into a bf16 operand tile;
@@ -45,9 +45,10 @@ constexpr int kMlaHeads = 16;
 constexpr int kMlaQkDim = kMlaLat + kMlaRope;
 constexpr int kT = 64;              // tokens per tile
 constexpr int kBoxes = kT / kBoxTokens;
-constexpr int kWorkers = 256;       // warps 0-1 softmax, 2-7 decode (2-3 also rescale O)
-constexpr int kDecoders = 192;      // warps 2-7
-constexpr int kMmaWarp = 8, kTmaWarp = 9;
+constexpr int kDecodeWarps = 8;     // decode warps 2..9 (2-3 also rescale O)
+constexpr int kDecoders = 32 * kDecodeWarps;
+constexpr int kWorkers = 64 + kDecoders;   // + softmax warps 0-1
+constexpr int kMmaWarp = kWorkers / 32, kTmaWarp = kMmaWarp + 1;
 constexpr int kThreads = kWorkers + 64;
 constexpr int kTmemCols = 128;      // S lat [2] @0,16 | S rope [2] @32,48 | O^T 4 x 16 @64
 constexpr int kColSLat = 0, kColSPe = 32, kColO = 64;
@@ -418,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================================================ workers
     // Q (decode warps): latent part as f16 (K-major [16 heads][512], 64-dim
     // atom columns 2 KB apart), rope part as bf16 ([16][64])
-    const int dt = tid - 64;   // decode thread 0..191
+    const int dt = tid - 64;   // decode thread 0..kDecoders-1
     if (warp >= 2) {
       const uint16_t* qg = a.q + (size_t)b * kMlaHeads * kMlaQkDim;
       for (int i = dt; i < kMlaHeads * (kMlaQkDim / 8); i += kDecoders) {
