@@ -13,16 +13,19 @@
 //
 // GB300 design.  One CTA per SM runs one chunk in tiles of 64 tokens with
 // warp-specialized roles that hand work over through mbarriers:
-//  * a TMA warp streams each tile's latent codes (128-byte swizzled boxes),
-//    block scales (1-D bulk copy) and rope keys into a two-stage ring;
+//  * TMA copies stream each tile's latent codes (128-byte swizzled boxes),
+//    block scales (1-D bulk copy) and rope keys into a two-stage ring; lane 0
+//    of the last decode warp issues them when a stage has been decoded;
 //  * eight decode warps turn a tile, once, into an f16 [token][dim] tile
 //    (E2M1 x E4M3 -> f16 is exact) in the 128-byte-swizzled layout that is
 //    the K-major A operand of S^T = K Q^T and, read MN-major, the A operand
 //    of O^T = V^T P^T; they copy the rope keys into a bf16 operand tile;
-//  * an MMA warp issues tcgen05.mma (kind::f16, M = 128, N = 16 heads): S^T
-//    of the latent (f16) and of the rope part (bf16) into two tensor-memory
-//    accumulators (their scales differ), O^T of four 128-dim blocks into a
-//    third, taking whichever tile is ready;
+//  * the MMAs are tcgen05.mma (kind::f16, M = 128, N = 16 heads): S^T of the
+//    latent (f16) and of the rope part (bf16) into two tensor-memory
+//    accumulators (their scales differ), and O^T of four 128-dim blocks into
+//    a third.  One thread issues S^T once a tile is decoded, another O^T once
+//    its P^T is written, so that one's wait and fence overlap the other's
+//    batch;
 //  * two softmax warps read S^T from tensor memory (one token per thread,
 //    all 16 heads), run the softmax with a lazily moving reference max and
 //    write P^T (f16) as the B operand of the O^T MMA.  When the reference
@@ -48,7 +51,7 @@ constexpr int kBoxes = kT / kBoxTokens;
 constexpr int kDecodeWarps = 8;     // decode warps 2..9 (2-3 also rescale O)
 constexpr int kDecoders = 32 * kDecodeWarps;
 constexpr int kWorkers = 64 + kDecoders;   // + softmax warps 0-1
-constexpr int kMmaWarp = kWorkers / 32, kTmaWarp = kMmaWarp + 1;
+constexpr int kSWarp = kWorkers / 32, kOWarp = kSWarp + 1;   // TMA + S^T issue, O^T issue
 constexpr int kThreads = kWorkers + 64;
 constexpr int kTmemCols = 128;      // S lat [2] @0,16 | S rope [2] @32,48 | O^T 4 x 16 @64
 constexpr int kColSLat = 0, kColSPe = 32, kColO = 64;
@@ -186,18 +189,6 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((c >> 3) ^ r) & 7) << 4) + (c & 7) * 2);
 }
 
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Bounded wait by the calling thread; a timeout raises the CTA's abort flag.
 __device__ __forceinline__ void wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   if (!mbar_wait(bar, parity)) *abort_flag = 1;
@@ -300,69 +291,60 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
   for (int h = 0; h < kMlaHeads; ++h) m[h] = -INFINITY, l[h] = 0.f;
 
-  // ============================================================ TMA warp
-  if (warp == kTmaWarp) {
-    if (lane == 0) {
-      auto fresh_wait = [&](int x) {
-        if (!dep_done && x * kT + kT > fresh_tok) {
-          griddep_wait();
-          dep_done = true;
-        }
-      };
-      // A tile inside one page moves as four copies (64-row boxes), otherwise
-      // as four per 16-token box.  Stage layout: codes [half][row][128 B]
-      // (128-byte swizzle), scales [row][32 B], rope keys [row][128 B].
-      auto issue_raw = [&](int x) {
-        fresh_wait(x);
-        const int nb = min(kBoxes, (ntok - x * kT + kBoxTokens - 1) / kBoxTokens);
-        const uint32_t st = base + kOffRaw + (x % kRawStages) * kRawStage;
-        const uint32_t bar = smem_u32(&sm.raw_full[x % kRawStages]);
-        constexpr uint32_t kRowBytes = kMlaLat / 2 + kMlaLat / 16 + kMlaRope * 2;   // 416
-        mbar_arrive_expect_tx(bar, nb * kBoxTokens * kRowBytes);
-        const int tok0 = cstart + x * kT;
-        const long row0 = cache_row(tok0);
-        if (nb == kBoxes && tok0 / a.ps == (tok0 + kT - 1) / a.ps) {
-          tma_load_3d(st, &tmCodes64, 0, 0, (int)row0, bar);
-          tma_load_3d(st + kRawCodes / 2, &tmCodes64, 0, 1, (int)row0, bar);
-          bulk_load(st + kRawCodes, a.k_bscale + row0 * (kMlaLat / 16), kT * (kMlaLat / 16), bar);
-          tma_load_2d(st + kRawCodes + kRawScales, &tmPe64, 0, (int)row0, bar);
-          return;
-        }
-        for (int k = 0; k < nb; ++k) {
-          const long row = k == 0 ? row0 : cache_row(tok0 + k * kBoxTokens);
-          tma_load_3d(st + k * 2048, &tmCodes, 0, 0, (int)row, bar);
-          tma_load_3d(st + kRawCodes / 2 + k * 2048, &tmCodes, 0, 1, (int)row, bar);
-          bulk_load(st + kRawCodes + k * (kBoxTokens * (kMlaLat / 16)),
-                    a.k_bscale + row * (kMlaLat / 16), kBoxTokens * (kMlaLat / 16), bar);
-          tma_load_2d(st + kRawCodes + kRawScales + k * 2048, &tmPe, 0, (int)row, bar);
-        }
-      };
-      int issued = 0;
-      for (; issued < nt; ++issued) {
-        // the stage of tile x was read by the decode of tile x - 2
-        if (issued >= kRawStages)
-          wait_bar(smem_u32(&sm.dec_ready[issued & 1]), ((issued - kRawStages) >> 1) & 1,
-                   abort_flag);
-        if (*abort_flag) break;
-        issue_raw(issued);
-      }
-      if (!dep_done) griddep_wait();   // the grid ends after the append it overlapped
-      for (int x = max(0, issued - kRawStages); x < issued; ++x)
-        mbar_wait(smem_u32(&sm.raw_full[x % kRawStages]), (x / kRawStages) & 1);
+  // Descriptors are built once; per MMA only the start-address field moves
+  // (16-byte units, no carry out of 14 bits: every shared address is below
+  // 256 KB).  Both buffer parities are precomputed.
+  const uint64_t dq = sdesc(base + kOffQLat, 16, 1024);
+  const uint64_t dqpe = sdesc(base + kOffQPe, 16, 1024);
+  const uint64_t dk0 = sdesc(base + kOffTile, 16, 1024);   // K-major tile
+  const uint64_t dk1 = sdesc(base + kOffTile + kTileBytes, 16, 1024);
+
+  // Copies of tile x into raw stage x % 2 (by lane 0 of the last decode
+  // warp).  A tile inside one page moves as four copies (64-row boxes),
+  // otherwise as four per 16-token box.  Stage layout: codes [half][row][128 B]
+  // (128-byte swizzle), scales [row][32 B], rope keys [row][128 B].
+  auto fresh_wait = [&](int x) {
+    if (!dep_done && x * kT + kT > fresh_tok) {
+      griddep_wait();
+      dep_done = true;
     }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ========================================================== MMA warp
-    int s_next = 0, o_next = 0;
+  };
+  auto issue_raw = [&](int x) {
+    fresh_wait(x);
+    const int nb = min(kBoxes, (ntok - x * kT + kBoxTokens - 1) / kBoxTokens);
+    const uint32_t st = base + kOffRaw + (x % kRawStages) * kRawStage;
+    const uint32_t bar = smem_u32(&sm.raw_full[x % kRawStages]);
+    constexpr uint32_t kRowBytes = kMlaLat / 2 + kMlaLat / 16 + kMlaRope * 2;   // 416
+    mbar_arrive_expect_tx(bar, nb * kBoxTokens * kRowBytes);
+    const int tok0 = cstart + x * kT;
+    const long row0 = cache_row(tok0);
+    if (nb == kBoxes && tok0 / a.ps == (tok0 + kT - 1) / a.ps) {
+      tma_load_3d(st, &tmCodes64, 0, 0, (int)row0, bar);
+      tma_load_3d(st + kRawCodes / 2, &tmCodes64, 0, 1, (int)row0, bar);
+      bulk_load(st + kRawCodes, a.k_bscale + row0 * (kMlaLat / 16), kT * (kMlaLat / 16), bar);
+      tma_load_2d(st + kRawCodes + kRawScales, &tmPe64, 0, (int)row0, bar);
+      return;
+    }
+    for (int k = 0; k < nb; ++k) {
+      const long row = k == 0 ? row0 : cache_row(tok0 + k * kBoxTokens);
+      tma_load_3d(st + k * 2048, &tmCodes, 0, 0, (int)row, bar);
+      tma_load_3d(st + kRawCodes / 2 + k * 2048, &tmCodes, 0, 1, (int)row, bar);
+      bulk_load(st + kRawCodes + k * (kBoxTokens * (kMlaLat / 16)),
+                a.k_bscale + row * (kMlaLat / 16), kBoxTokens * (kMlaLat / 16), bar);
+      tma_load_2d(st + kRawCodes + kRawScales + k * 2048, &tmPe, 0, (int)row, bar);
+    }
+  };
+
+  // ================================================== S^T issue (one thread)
+  if (warp == kSWarp) {
     if (lane == 0) {
-      // Descriptors are built once; per MMA only the start-address field
-      // moves (16-byte units, no carry out of 14 bits: every shared address
-      // is below 256 KB).
-      const uint64_t dq = sdesc(base + kOffQLat, 16, 1024);
-      const uint64_t dqpe = sdesc(base + kOffQPe, 16, 1024);
+      const uint64_t dpe0 = sdesc(base + kOffPe, 16, 1024);
+      const uint64_t dpe1 = sdesc(base + kOffPe + kPeBytes, 16, 1024);
+      // S^T MMA x: tile x decoded.  Its S^T buffer was read by the softmax of
+      // x - 2, which precedes O^T x - 2, which precedes the decode of x.
       auto issue_s = [&](int x) {
-        const uint64_t da = sdesc(base + kOffTile + (x & 1) * kTileBytes, 16, 1024);
-        const uint64_t dpe = sdesc(base + kOffPe + (x & 1) * kPeBytes, 16, 1024);
+        const uint64_t da = (x & 1) ? dk1 : dk0;
+        const uint64_t dpe = (x & 1) ? dpe1 : dpe0;
         const uint32_t dl = tmem + kColSLat + 16 * (x & 1), dp = tmem + kColSPe + 16 * (x & 1);
 #pragma unroll
         for (int kk = 0; kk < kMlaLat / 16; ++kk)
@@ -373,9 +355,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma(dp, dpe + (uint64_t)(kk * 2), dqpe + (uint64_t)(kk * 2), kIdBf16, kk > 0);
         mma_commit(smem_u32(&sm.s_done[x & 1]));
       };
+      int s_issued = 0;
+      for (int x = 0; x < nt; ++x) {
+        wait_bar(smem_u32(&sm.dec_ready[x & 1]), (x >> 1) & 1, abort_flag);
+        if (*abort_flag) break;
+        tc_fence_after();
+        issue_s(x);
+        ++s_issued;
+      }
+      // every MMA of this thread has completed at exit (bounded waits)
+      for (int x = max(0, s_issued - 2); x < s_issued; ++x)
+        mbar_wait(smem_u32(&sm.s_done[x & 1]), (x >> 1) & 1);
+      if (s_issued < nt) *abort_flag = 1;
+    }
+    __syncwarp();
+  } else if (warp == kOWarp) {
+    // ============================================== O^T issue (one thread)
+    if (lane == 0) {
+      const uint64_t dv0 = sdesc(base + kOffTile, 8192, 1024);   // MN-major tile
+      const uint64_t dv1 = sdesc(base + kOffTile + kTileBytes, 8192, 1024);
+      const uint64_t dpt0 = sdesc(base + kOffP, 16, 1024);
+      const uint64_t dpt1 = sdesc(base + kOffP + kPBytes, 16, 1024);
+      // O^T MMA x: P^T x written and O rescaled (which implies S^T x done)
       auto issue_o = [&](int x) {
-        const uint64_t da = sdesc(base + kOffTile + (x & 1) * kTileBytes, 8192, 1024);
-        const uint64_t dpt = sdesc(base + kOffP + (x & 1) * kPBytes, 16, 1024);
+        const uint64_t da = (x & 1) ? dv1 : dv0;
+        const uint64_t dpt = (x & 1) ? dpt1 : dpt0;
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
 #pragma unroll
@@ -384,35 +388,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dpt + (uint64_t)(kk * 2), kIdF16MnA, x > 0 || kk > 0);
         mma_commit(smem_u32(&sm.o_done[x & 1]));
       };
-      // S^T MMA x: tile x decoded, and its S^T buffer read by the softmax of
-      // x-2 (whose P^T made O^T x-2 issuable); O^T MMA x: P^T x written (and
-      // O rescaled).  Whichever is ready goes first; the O^T MMA is preferred
-      // (the decode of tile x+2 waits for it).
-      uint64_t t0 = globaltimer_ns();
-      while (o_next < nt && !*abort_flag) {
-        if (o_next < s_next &&
-            mbar_test(smem_u32(&sm.p_ready[o_next & 1]), (o_next >> 1) & 1)) {
-          tc_fence_after();
-          issue_o(o_next);
-          ++o_next;
-          t0 = globaltimer_ns();
-        } else if (s_next < nt && s_next <= o_next + 1 &&
-                   mbar_test(smem_u32(&sm.dec_ready[s_next & 1]), (s_next >> 1) & 1)) {
-          tc_fence_after();
-          issue_s(s_next);
-          ++s_next;
-          t0 = globaltimer_ns();
-        } else if (globaltimer_ns() - t0 > 250000000ull) {
-          *abort_flag = 1;
-        }
+      int o_issued = 0;
+      for (int x = 0; x < nt; ++x) {
+        wait_bar(smem_u32(&sm.p_ready[x & 1]), (x >> 1) & 1, abort_flag);
+        if (*abort_flag) break;
+        tc_fence_after();
+        issue_o(x);
+        ++o_issued;
       }
-      // every MMA issued has completed (bounded waits)
-      for (int x = max(0, s_next - 2); x < s_next; ++x)
-        mbar_wait(smem_u32(&sm.s_done[x & 1]), (x >> 1) & 1);
       bool ok = true;
-      for (int x = max(0, o_next - 2); x < o_next; ++x)
+      for (int x = max(0, o_issued - 2); x < o_issued; ++x)
         ok &= mbar_wait(smem_u32(&sm.o_done[x & 1]), (x >> 1) & 1);
-      if (!ok || o_next < nt) *abort_flag = 1;
+      if (!ok || o_issued < nt) *abort_flag = 1;
     }
     __syncwarp();
   } else {
@@ -420,17 +407,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Q (decode warps): latent part as f16 (K-major [16 heads][512], 64-dim
     // atom columns 2 KB apart), rope part as bf16 ([16][64])
     const int dt = tid - 64;   // decode thread 0..kDecoders-1
+    // lane 0 of the last decode warp issues the copies: tiles 0 and 1 first
+    // (before the Q loads), tile y + 2 when every decode thread is done with y
+    const bool tma_thread = warp == kWorkers / 32 - 1 && lane == 0;
+    int issued = 0;
+    if (tma_thread)
+      for (; issued < min(nt, kRawStages); ++issued) issue_raw(issued);
     if (warp >= 2) {
+      // all of a thread's loads first: after an L2 flush each is a DRAM trip
+      constexpr int kQItems = kMlaHeads * (kMlaQkDim / 8);
+      constexpr int kQPer = (kQItems + kDecoders - 1) / kDecoders;
       const uint16_t* qg = a.q + (size_t)b * kMlaHeads * kMlaQkDim;
-      for (int i = dt; i < kMlaHeads * (kMlaQkDim / 8); i += kDecoders) {
+      uint4 qv[kQPer];
+#pragma unroll
+      for (int k = 0; k < kQPer; ++k) {
+        const int i = dt + k * kDecoders;
+        if (i < kQItems)
+          qv[k] = *reinterpret_cast<const uint4*>(qg + (size_t)(i / (kMlaQkDim / 8)) * kMlaQkDim +
+                                                  (i % (kMlaQkDim / 8)) * 8);
+      }
+#pragma unroll
+      for (int k = 0; k < kQPer; ++k) {
+        const int i = dt + k * kDecoders;
+        if (i >= kQItems) break;
         const int h = i / (kMlaQkDim / 8), d = (i % (kMlaQkDim / 8)) * 8;
-        const uint4 v = *reinterpret_cast<const uint4*>(qg + (size_t)h * kMlaQkDim + d);
+        const uint4 v = qv[k];
         if (d < kMlaLat) {
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
           uint32_t f[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            f[k] = pack_f16x2(bf16_bits_to_f32(w[k] & 0xFFFFu), bf16_bits_to_f32(w[k] >> 16));
+          for (int j = 0; j < 4; ++j)
+            f[j] = pack_f16x2(bf16_bits_to_f32(w[j] & 0xFFFFu), bf16_bits_to_f32(w[j] >> 16));
           sts128(base + kOffQLat + (d >> 6) * 2048 + swz(h, d & 63), f[0], f[1], f[2], f[3]);
         } else {
           sts128(base + kOffQPe + swz(h, d - kMlaLat), v.x, v.y, v.z, v.w);
@@ -447,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t st = base + kOffRaw + (x % kRawStages) * kRawStage;
       const uint32_t tile = base + kOffTile + (x & 1) * kTileBytes;
       const int nvalid = min(kT, ntok - x * kT);
-#pragma unroll 1
+#pragma unroll 2
       for (int u = dt; u < kT * 16; u += kDecoders) {
         const int p = u & 7, rest = u >> 3;
         const int rg = rest >> 4, db = (rest & 15) >> 1, half = rest & 1;
@@ -514,9 +521,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp >= 2) {
       // ---- decode warps: tile t+1 (its buffer was last read by O^T MMA
       // t-1); warps 2-3 also take lanes 64..127 of an O rescale of tile t
+      auto refill = [&](int y) {
+        if (tma_thread && issued < nt) {
+          wait_bar(smem_u32(&sm.dec_ready[y & 1]), (y >> 1) & 1, abort_flag);
+          if (!*abort_flag) issue_raw(issued++);
+        }
+      };
       if (nt > 0) {
         wait_bar(smem_u32(&sm.raw_full[0]), 0, abort_flag);
         decode(0);
+        refill(0);
       }
       int nresc = 0;
       for (int t = 0; t < nt && !*abort_flag; ++t) {
@@ -525,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           wait_bar(smem_u32(&sm.raw_full[(t + 1) % kRawStages]), ((t + 1) / kRawStages) & 1,
                    abort_flag);
           decode(t + 1);
+          refill(t + 1);
         }
         if (warp < 4) {
           wait_bar(smem_u32(&sm.p_done[t & 1]), (t >> 1) & 1, abort_flag);
@@ -534,6 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++nresc;
           }
         }
+      }
+      if (tma_thread) {
+        if (!dep_done) griddep_wait();   // the grid ends after the append it overlapped
+        // no copy in flight at exit (bounded waits)
+        for (int x = max(0, issued - kRawStages); x < issued; ++x)
+          mbar_wait(smem_u32(&sm.raw_full[x % kRawStages]), (x / kRawStages) & 1);
       }
     } else {
       // ---- softmax warps: tile t, one token per thread, all 16 heads
