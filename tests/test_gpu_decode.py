@@ -147,6 +147,31 @@ def test_large_groups_fp8_probs():
         assert_f32_close(out.cpu().numpy(), ref, f"G=16 probs s={s}")
 
 
+@pytest.mark.parametrize("shape", ["gqa4_d128", "gqa4_d64", "nvfp4_d128"])
+def test_fp8_probs_shapes(shape):
+    """FP8 probabilities beyond MHA: four query heads per kv head at head_dim
+    128 and 64 with an FP8 cache, and with an NVFP4 cache; ragged lengths,
+    several splits."""
+    if shape == "gqa4_d128":
+        w = synth.gqa_fp8(700)
+        w.B, w.Hq, w.Hkv = 2, 8, 2
+        w.seq_lens = np.array([700, 333], np.int32)
+    elif shape == "gqa4_d64":
+        w = synth.tiny_fp8(300)
+        w.B = 3
+        w.seq_lens = np.array([300, 77, 16], np.int32)
+    else:
+        w = synth.nvfp4(500)
+        w.B, w.Hq, w.Hkv = 2, 8, 2
+        w.seq_lens = np.array([500, 129], np.int32)
+    w.prob_fp8 = True
+    S = Setup(w)
+    for s in (1, 3):
+        ref, _ = S.oracle_decode(mode=1, s=s)
+        out, _ = S.gpu_decode(s)
+        assert_f32_close(out.cpu().numpy(), ref, f"{shape} probs s={s}")
+
+
 def test_edge_lengths():
     """Lengths 0 (output 0), 1, 15, 16, 17 and fewer tokens than splits."""
     w = synth.gqa_fp8(64)
