@@ -191,8 +191,10 @@ kvq_status kvq_quantize_append(const kvq_cache* c, const void* k_new, const void
  * shape: KVQ_NVFP4, num_kv_heads 1, q_per_kv 16), so
  * floor(ctas_per_sm * num_sms / base) splits fill one wave;
  * s is at least ceil(max_kv_len / 2048), so that long or ragged requests
- * are cut into chunks that balance across waves.  s is then lowered so that
- * every chunk keeps at least 128 tokens and clamped to [1, 64].  num_sms is
+ * are cut into chunks that balance across waves.  Above 32 splits with
+ * chunks under 256 tokens (max_kv_len < 256 s), s becomes
+ * max(32, ceil(max_kv_len / 256)).  s is then lowered so that every chunk
+ * keeps at least 128 tokens and clamped to [1, 64].  num_sms is
  * the device's multiprocessor count (cudaDevAttrMultiProcessorCount).
  */
 kvq_status kvq_auto_splits(int num_sms, int batch, int num_kv_heads, int q_per_kv,

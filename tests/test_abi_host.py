@@ -68,6 +68,12 @@ def test_auto_splits():
     assert f(152, 2, 8, 4, 100, 1) == (0, 1)
     # batch 1 x 8 kv heads: floor(456 / 8) = 57
     assert f(152, 1, 8, 4, 32768, 2) == (0, 57)
+    assert f(152, 1, 8, 4, 16384, 2) == (0, 57)
+    # more than 32 splits of chunks under 256 tokens: max(32, ceil(L / 256))
+    assert f(152, 1, 8, 4, 14336, 2) == (0, 56)
+    assert f(152, 1, 8, 4, 12288, 2) == (0, 48)
+    assert f(152, 1, 8, 4, 8192, 2) == (0, 32)
+    assert f(152, 1, 8, 4, 8192, 1) == (0, 32)
     assert f(152, 1, 8, 4, 2048, 2) == (0, 16)
     # large batch: chunks of at most 2048 tokens (ceil(8192 / 2048) = 4)
     assert f(152, 64, 16, 1, 8192, 1) == (0, 4)
