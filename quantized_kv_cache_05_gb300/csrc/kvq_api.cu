@@ -20,7 +20,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  // The driver entry point is looked up once per process.
+  // The CUDA driver API entry point is looked up once per process.
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
