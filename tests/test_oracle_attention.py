@@ -202,6 +202,28 @@ def test_probq_batch_uses_chunks(orc):
     assert np.allclose(out[0, 0], exact, atol=0.1)     # same answer up to FP8 weights
 
 
+@pytest.mark.parametrize("s", [1, 2, 3, 5])
+def test_probq_powers_of_two_are_lossless(orc, s):
+    """Weights 2^-n (0 <= n <= 14 below each chunk's max) quantize without
+    loss: p~ / prob_scale = 1.75 * 2^(8 - n) is an E4M3 value, so the FP8
+    probability mode equals exact attention up to the fp32 rounding of
+    prob_scale itself (relative ~3e-8), for any split count.  A dropped or
+    doubled prob_scale, a wrong chunk max or a broken chunk merge fails."""
+    L, Dv = 40, 6
+    rng = np.random.default_rng(41)
+    n = rng.integers(0, 12, L)
+    n[rng.integers(0, L)] = 0
+    q = np.array([[[1.0]]])
+    k = (-(n.astype(np.float64)) * math.log(2.0)).reshape(1, 1, L, 1)
+    v = rng.standard_normal((1, 1, L, Dv))
+    out, _ = orc.decode_batch(q, k, v, np.array([L]), 1.0, mode=1, s=s, prob_scale=PS)
+    exact, _ = orc.attention_exact(q[0, 0], k[0, 0], v[0, 0], 1.0)
+    w = np.exp2(-n.astype(np.float64))
+    closed = (w[:, None] * v[0, 0]).sum(axis=0) / w.sum()
+    assert np.allclose(exact, closed, rtol=0, atol=1e-12)
+    assert np.allclose(out[0, 0], closed, rtol=0, atol=1e-7 * np.abs(v).max())
+
+
 def test_fp8_output(orc):
     o = np.array([1.0, -2.0, 500.0, 0.0])
     assert list(orc.fp8_output(o, 1.0)) == [0x38, 0xC0, 0x7E, 0x00]
