@@ -337,7 +337,7 @@ kvq_status kvq_decode(const kvq_cache* c, const kvq_decode_params* p, const void
                       float* part_o, float* part_lse, uint32_t* counters, void* out,
                       void* stream) {
   if (p && p->batch > 0 && (!counters || !out)) return KVQ_ERR_INVALID;
-  return decode_impl(c, p, q, part_o, part_lse, counters ? counters : nullptr, out,
+  return decode_impl(c, p, q, part_o, part_lse, counters, out,
                      as_stream(stream));
 }
 
