@@ -612,31 +612,54 @@ Bench.with_splits = _with_splits
 # the CPU oracle (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_step_time(w, groups, nthreads):
+def oracle_step_time(w, groups, nthreads, s=1):
     """Seconds for the oracle's decode step on the given (request, kv head)
-    groups: dequantize the group's cached codes and run exact attention for
-    its query heads.  Quantization of the cache is setup, not timed."""
+    groups: dequantize the group's cached codes (FP8, or NVFP4; MLA: the
+    latent plus the bf16 rope keys) and run exact attention for its query
+    heads, or the FP8-probability reading with s splits.  Quantizing the cache
+    is setup and not timed; the per-tensor scales come from the sampled
+    requests."""
     import concurrent.futures
     import oracle
     from quantized_kv_cache_05_gb300 import synth
 
     q = synth.bf16_to_f32(w.q()).astype(np.float64)
-    amax_k = max(oracle.amax_bf16(w.kv_rows(synth.T_K, b)) for b in range(w.B))
-    amax_v = max(oracle.amax_bf16(w.kv_rows(synth.T_V, b)) for b in range(w.B))
-    ks, vs = oracle.fp8_tensor_scale(amax_k), oracle.fp8_tensor_scale(amax_v)
+    reqs = sorted({b for b, _ in groups})
+    k_rows = {b: w.kv_rows(synth.T_K, b) for b in reqs}
+    v_rows = None if w.mla else {b: w.kv_rows(synth.T_V, b) for b in reqs}
+    tensor_scale = oracle.fp8_tensor_scale if w.fmt == "fp8" else oracle.nvfp4_global_scale
+    ks = tensor_scale(max(oracle.amax_bf16(k_rows[b]) for b in reqs))
+    vs = ks if w.mla else tensor_scale(max(oracle.amax_bf16(v_rows[b]) for b in reqs))
+
+    def quant(x, scale):
+        return (oracle.fp8_quantize(x, scale), None) if w.fmt == "fp8" else \
+            oracle.nvfp4_quantize(x, scale)
+
+    def dequant(cb, scale):
+        codes, bs = cb
+        return oracle.fp8_dequant(codes, scale) if w.fmt == "fp8" else \
+            oracle.nvfp4_dequant(codes, bs, scale)
+
     codes = {}
     for b, h in groups:
-        codes[(b, h)] = (oracle.fp8_quantize(w.kv_rows(synth.T_K, b)[:, h], ks),
-                         oracle.fp8_quantize(w.kv_rows(synth.T_V, b)[:, h], vs))
+        kc = quant(k_rows[b][:, h], ks)
+        vc = None if w.mla else quant(v_rows[b][:, h], vs)
+        kpe = w.kpe_rows(b) if w.mla else None
+        codes[(b, h)] = (kc, vc, kpe)
+    mode = 1 if w.prob_fp8 else 0
 
     def one(bh):
         b, h = bh
-        kc, vc = codes[bh]
-        kh = oracle.fp8_dequant(kc, ks)
-        vh = oracle.fp8_dequant(vc, vs)
+        kc, vc, kpe = codes[bh]
+        kh = dequant(kc, ks)
+        if w.mla:
+            vh = kh
+            kh = np.concatenate([kh, synth.bf16_to_f32(kpe).astype(np.float64)], axis=1)
+        else:
+            vh = dequant(vc, vs)
         qs = q[b, h * w.G:(h + 1) * w.G][None]
         oracle.decode_batch(qs, kh[None, None], vh[None, None], np.array([kh.shape[0]]),
-                            w.sm_scale, nthreads=1)
+                            w.sm_scale, mode=mode, s=s, prob_scale=w.prob_scale, nthreads=1)
 
     t0 = time.perf_counter()
     with concurrent.futures.ThreadPoolExecutor(nthreads) as ex:
@@ -646,14 +669,15 @@ def oracle_step_time(w, groups, nthreads):
 
 def cpu_baseline(w, bench=None, seconds=10.0):
     nthreads = os.cpu_count() or 1
+    s = bench.splits if (bench is not None and w.prob_fp8) else 1
     all_groups = [(b, h) for b in range(w.B) for h in range(w.Hkv)]
     # size the sample: time one group, then take as many as fit the budget
-    t1 = oracle_step_time(w, all_groups[:1], 1)
+    t1 = oracle_step_time(w, all_groups[:1], 1, s)
     n = int(max(1, min(len(all_groups), seconds / max(t1, 1e-6) * nthreads / 2)))
     sample = all_groups[:n]
     reps, tot = 0, 0.0
     while tot < seconds / 2 and reps < 50:
-        tot += oracle_step_time(w, sample, nthreads)
+        tot += oracle_step_time(w, sample, nthreads, s)
         reps += 1
     per_step = tot / reps * len(all_groups) / len(sample)
     return {"value": round(per_step * 1e6, 1), "unit": "us/step", "cores": nthreads,
@@ -663,11 +687,14 @@ def cpu_baseline(w, bench=None, seconds=10.0):
 
 
 def run_reference(args):
-    from quantized_kv_cache_05_gb300 import synth
+    """The oracle, as it stands, on this arm's workload (host cores; rank 0
+    only).  FP8-probability mode is timed with one chunk per request: the
+    oracle's work per token does not depend on the split count."""
     rank = env_int("RANK", 0)
     if rank != 0:
         return
-    w = synth.gqa_fp8(args.kv_len)
+    spec = WORKLOADS[args.workload]
+    w = spec["make"](args.kv_len)
     nthreads = os.cpu_count() or 1
     groups = [(b, h) for b in range(w.B) for h in range(w.Hkv)]
     t1 = oracle_step_time(w, groups[:1], 1)
@@ -680,13 +707,13 @@ def run_reference(args):
     us = statistics.mean(times) * 1e6
     line = {
         "impl": "reference",
-        "metric": METRIC, "value": round(us, 1), "unit": "us/step", "n_gpus": 0,
+        "metric": METRIC, "value": round(us, 1), "unit": "us/step", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded bf16 N(0,1), 1% x10 outliers)",
-        "config": {"workload": f"gqa_fp8: batch 2, Hq 32, Hkv 8, head_dim 128, kv_len "
-                               f"{args.kv_len}, FP8 E4M3 per-tensor KV", "batch": w.B,
-                   "kv_len": args.kv_len},
+        "data": spec["data"],
+        "config": {"workload": spec["desc"](w), "batch": w.B, "kv_len": int(w.Lmax),
+                   "step": "fp64 oracle: dequantize the cache, attention per (request, kv head)",
+                   "parallelism": f"{nthreads} host threads"},
         "cpu_baseline": {"value": round(us, 1), "unit": "us/step", "cores": nthreads,
                          "kind": "oracle",
                          "sample": f"{len(sample)} of {len(groups)} (request, kv head) groups "
