@@ -135,7 +135,7 @@ typedef struct kvq_decode_params {
    * complete when that call was made (kvq_quantize_append starts after all
    * earlier work in the stream).  The decode then streams every other part
    * of the cache while the append runs and waits for it only before the
-   * boxes that hold those positions.  Not part of the papers' method: a
+   * boxes that hold those positions.  Not part of the pages' method: a
    * scheduling contract between two calls of this library.
    */
   int32_t fresh_tokens;
@@ -251,7 +251,7 @@ kvq_status kvq_decode(const kvq_cache* c, const kvq_decode_params* p, const void
                       void* stream);
 
 /*
- * Allocation-free decode step (the paper has no counterpart; this is a
+ * Allocation-free decode step (the pages have no counterpart; this is a
  * convenience of this library).  For callers that cannot allocate device
  * memory -- their device memory is owned by a host framework's fixed pool,
  * or a hard memory budget forbids another cudaMalloc -- this does what
