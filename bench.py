@@ -407,17 +407,27 @@ class Bench:
             per = 2 * w.Hkv * row
         return tok * per
 
-    def partial_bytes(self) -> int:
-        """Algorithmic bytes of one kvq_decode launch: attended cache bytes,
-        block-table entries and Q read; split partials written and read back
-        by the merging CTA; the output written."""
+    def table_bytes(self) -> int:
+        """Block-table entries the decode reads: one 4-byte entry per page of
+        each request, once per kv head (each (request, kv head) CTA group
+        reads its own chunks' entries)."""
         w = self.w
         ps = w.page_size_eff()
-        bt = int(sum(-(-int(L) // ps) for L in w.seq_lens)) * 4 * (1 if w.mla else w.Hkv)
-        q = w.B * w.Hq * w.Dqk * 2
-        parts = 2 * w.B * w.Hq * self.splits * (w.Dv + 1) * 4
-        out = w.B * w.Hq * w.Dv * self.ws.out.element_size()
-        return self.kv_bytes() + bt + q + parts + out
+        pages = int(sum(-(-int(L) // ps) for L in w.seq_lens))
+        return pages * 4 * (1 if w.mla else w.Hkv)
+
+    def algorithmic_bytes(self) -> int:
+        """Algorithmic HBM bytes of one decode launch: the attended cache
+        bytes (codes, block scales, rope keys) and the block-table entries.
+        The split partials, q and the output are reported separately."""
+        return self.kv_bytes() + self.table_bytes()
+
+    def side_bytes(self) -> dict:
+        """Bytes one kvq_decode launch moves besides the algorithmic ones."""
+        w = self.w
+        return {"split_partials": 2 * w.B * w.Hq * self.splits * (w.Dv + 1) * 4,
+                "q": w.B * w.Hq * w.Dqk * 2,
+                "out": w.B * w.Hq * w.Dv * self.ws.out.element_size()}
 
 
 def _workloads():
@@ -491,7 +501,7 @@ def run_ours(args):
     # call between two events on its stream (the graph-replayed figure is
     # reported beside it and carries the graph launch on top)
     part = statistics.mean(part_plain_us)
-    achieved = bench.partial_bytes() / (part * 1e-6) / 1e9
+    achieved = bench.algorithmic_bytes() / (part * 1e-6) / 1e9
     traffic = ncu_traffic(w.name, spec["kind"])
     kvb = bench.kv_bytes()
     line = {
@@ -529,7 +539,9 @@ def run_ours(args):
             "peak_kind": peak_kind,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "algorithmic_bytes_per_launch": bench.partial_bytes(),
+            "algorithmic_bytes_per_launch": bench.algorithmic_bytes(),
+            "algorithmic_bytes": "attended KV codes + block scales + rope keys + block-table entries",
+            "other_bytes_per_launch": bench.side_bytes(),
             "traffic": traffic,
         },
         "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": bi,
@@ -584,11 +596,15 @@ def sweep(device, args):
                 base = base or b
                 st = b.time_graph(b.graph_step, args.sweep_steps, 3)
                 us = statistics.mean(st)
+                ku = statistics.mean(b.time_plain(False, args.sweep_steps, 3))
                 kvb = b.kv_bytes()
+                ab = b.algorithmic_bytes()
                 res.append({"workload": name, "kv_len": L or int(w.Lmax), "s": s or "auto",
                             "splits": b.splits, "us_per_step": round(us, 2),
                             "kv_gbs": round(kvb / (us * 1e-6) / 1e9, 1),
-                            "kv_hbm_frac": round(kvb / (us * 1e-6) / 1e9 / peak, 3)})
+                            "kv_hbm_frac": round(kvb / (us * 1e-6) / 1e9 / peak, 3),
+                            "kernel_us": round(ku, 2),
+                            "kernel_hbm_frac": round(ab / (ku * 1e-6) / 1e9 / peak, 3)})
             del base
     return res
 
@@ -614,11 +630,11 @@ Bench.with_splits = _with_splits
 
 def oracle_step_time(w, groups, nthreads, s=1):
     """Seconds for the oracle's decode step on the given (request, kv head)
-    groups: dequantize the group's cached codes (FP8, or NVFP4; MLA: the
-    latent plus the bf16 rope keys) and run exact attention for its query
-    heads, or the FP8-probability reading with s splits.  Quantizing the cache
-    is setup and not timed; the per-tensor scales come from the sampled
-    requests."""
+    groups: quantize the step's new K/V row (the one-token append), dequantize
+    the group's cached codes (FP8, or NVFP4; MLA: the latent plus the bf16 rope
+    keys) and run exact attention for its query heads, or the FP8-probability
+    reading with s splits.  Quantizing the rest of the cache is setup and not
+    timed; the per-tensor scales come from the sampled requests."""
     import concurrent.futures
     import oracle
     from quantized_kv_cache_05_gb300 import synth
@@ -648,8 +664,16 @@ def oracle_step_time(w, groups, nthreads, s=1):
         codes[(b, h)] = (kc, vc, kpe)
     mode = 1 if w.prob_fp8 else 0
 
+    # the step's append: the new token's K/V row of each group (its last row)
+    new_rows = {(b, h): (k_rows[b][-1:, h], None if w.mla else v_rows[b][-1:, h])
+                for b, h in groups}
+
     def one(bh):
         b, h = bh
+        kn, vn = new_rows[bh]
+        quant(kn, ks)
+        if vn is not None:
+            quant(vn, vs)
         kc, vc, kpe = codes[bh]
         kh = dequant(kc, ks)
         if w.mla:
@@ -683,7 +707,8 @@ def cpu_baseline(w, bench=None, seconds=10.0):
     return {"value": round(per_step * 1e6, 1), "unit": "us/step", "cores": nthreads,
             "kind": "oracle",
             "sample": f"{len(sample)} of {len(all_groups)} (request, kv head) groups, "
-                      f"{reps} repetitions, scaled to the whole step"}
+                      f"{reps} repetitions, scaled to the whole step; each group: quantize "
+                      f"its new K/V row, dequantize its cache, exact attention"}
 
 
 def run_reference(args):

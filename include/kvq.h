@@ -135,8 +135,10 @@ typedef struct kvq_decode_params {
    * complete when that call was made (kvq_quantize_append starts after all
    * earlier work in the stream).  The decode then streams every other part
    * of the cache while the append runs and waits for it only before the
-   * boxes that hold those positions.  Not part of the pages' method: a
-   * scheduling contract between two calls of this library.
+   * boxes that hold those positions.  q, seq_lens and the block table are
+   * read before that wait, so the append (or anything else still running
+   * when the decode starts) must not write them.  Not part of the pages'
+   * method: a scheduling contract between two calls of this library.
    */
   int32_t fresh_tokens;
 } kvq_decode_params;
@@ -178,7 +180,8 @@ kvq_status kvq_amax_bf16(const void* x /* device bf16 [n] */, size_t n,
  * The caller guarantees that the pages for positions start_pos[b] ..
  * start_pos[b] + n_tokens - 1 exist in the block table; positions past
  * max_pages_per_seq * page_size are skipped (not written).
- * Input pointers must be 16-byte aligned.
+ * Input pointers must be 16-byte aligned.  batch <= 32767, num_kv_heads <=
+ * 65535 and n_tokens < 2^30 (else KVQ_ERR_UNSUPPORTED).
  */
 kvq_status kvq_quantize_append(const kvq_cache* c, const void* k_new, const void* v_new,
                                const void* kpe_new, const int32_t* start_pos, int batch,
@@ -263,10 +266,14 @@ kvq_status kvq_decode(const kvq_cache* c, const kvq_decode_params* p, const void
  *   (4 * batch * Hq * num_splits) + 4 * batch * Hq * num_splits * v_dim
  *   bytes <= KVQ_NOALLOC_SCRATCH_BYTES; larger requests return
  *   KVQ_ERR_WORKSPACE (use kvq_decode with caller-owned buffers).
- *   The first call on a device looks up the buffer's device address
- *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Every call looks up the buffer's device address on the current device
+ *   (cudaGetSymbolAddress); the first call on a device also loads the
+ *   library's device code there, so make it before any stream capture.
  *   Every call clears the counters (an asynchronous memset on `stream`)
- *   and then launches the decode; it allocates and frees nothing.
+ *   and then launches the decode; it allocates and frees nothing.  The
+ *   memset sits between a preceding kvq_quantize_append and the decode, so
+ *   p->fresh_tokens > 0 is accepted but gives no overlap here: the decode
+ *   starts after the append has finished.
  *   All calls share the one buffer: calls that overlap on the GPU (other
  *   streams, other host threads) race and must be serialized by the caller.
  */
@@ -282,6 +289,23 @@ kvq_status kvq_decode_noalloc(const kvq_cache* c, const kvq_decode_params* p, co
  */
 kvq_status kvq_encode_e4m3(const float* x, uint8_t* out, size_t n, void* stream);
 kvq_status kvq_encode_e2m1(const float* x, uint8_t* out, size_t n, void* stream);
+
+/*
+ * The FP8-probability quantizer of the decode kernels (vLLM PR 15734:
+ * softmax(QK^T) quantized to FP8 with prob_output_scale), elementwise:
+ *   out[i] = E4M3(fl32(p[i] / prob_scale))   (round to nearest even, +-448)
+ * computed exactly as kvq_decode_partial computes it for probabilities in
+ * [0, 1].  The division by prob_scale takes a precomputed reciprocal and one
+ * fused correction when a host check shows that, for this prob_scale, it
+ * gives the codes of the IEEE division for every p in [0, 1] (it always does
+ * near the E4M3 rounding boundaries, where it is checked, and it is within
+ * one fp32 step of the IEEE quotient everywhere); otherwise it is the IEEE
+ * division.  *used_reciprocal (host, optional) tells which.  prob_scale
+ * finite > 0; p and out (device), n >= 0 (n = 0 runs only the host check).
+ * Codes for p outside [0, 1] are unspecified.
+ */
+kvq_status kvq_encode_prob_e4m3(const float* p, uint8_t* out, size_t n, float prob_scale,
+                                int* used_reciprocal /* host */, void* stream);
 
 #ifdef __cplusplus
 }

@@ -69,11 +69,15 @@ def _declare(L: ctypes.CDLL) -> None:
         "orc_e2m1_encode_n": (None, [_P, _sz, _P]),
         "orc_count_encode_mismatch": (_u64, [_i, _u64, _u64, _P, _i, _P]),
         "orc_bruteforce_encode_check": (_u64, [_i, _u64, _u64, _i, _P]),
+        "orc_count_probq_mismatch": (_u64, [_u64, _u64, _f, _P, _i, _P]),
         "orc_amax_bf16": (_f, [_P, _sz]),
         "orc_fp8_tensor_scale": (_f, [_f]),
         "orc_nvfp4_global_scale": (_f, [_f]),
         "orc_fp8_quantize": (None, [_P, _sz, _f, _P]),
         "orc_nvfp4_quantize": (None, [_P, _sz, _i, _f, _P, _P]),
+        "orc_head_amax_bf16": (None, [_P, _sz, _i, _i, _P]),
+        "orc_fp8_quantize_heads": (None, [_P, _sz, _i, _i, _P, _P]),
+        "orc_nvfp4_quantize_heads": (None, [_P, _sz, _i, _i, _P, _P, _P]),
         "orc_fp8_dequant": (None, [_P, _sz, _f, _P]),
         "orc_nvfp4_dequant": (None, [_P, _P, _sz, _i, _f, _P]),
         "orc_chunk": (None, [_i, _i, _i, _P, _P]),
@@ -149,6 +153,19 @@ def count_encode_mismatch(kind: int, first: int, observed: np.ndarray,
     return int(n), int(fb.value)
 
 
+def count_probq_mismatch(first: int, prob_scale: float, observed: np.ndarray,
+                         nthreads: int | None = None) -> tuple[int, int]:
+    """Compare observed codes for fp32 patterns [first, first+len), read as
+    probabilities p, with E4M3(fl32(p / prob_scale)) (the FP8-probability
+    step of vLLM PR 15734 as attention_partial_probq applies it).  Returns
+    (mismatches, first bad pattern or 2**64-1)."""
+    observed = _c(observed, np.uint8)
+    fb = ctypes.c_uint64(0)
+    n = lib().orc_count_probq_mismatch(first, observed.size, prob_scale, _ptr(observed),
+                                       nthreads or default_threads(), ctypes.byref(fb))
+    return int(n), int(fb.value)
+
+
 def bruteforce_encode_check(kind: int, first: int, n: int,
                             nthreads: int | None = None) -> tuple[int, int]:
     """Nearest-value table search vs the encoder over fp32 patterns."""
@@ -195,6 +212,53 @@ def nvfp4_quantize(x_bf16: np.ndarray, g: float) -> tuple[np.ndarray, np.ndarray
     codes = np.empty(x.shape[:-1] + (D // 2,), np.uint8)
     sc = np.empty(x.shape[:-1] + (D // 16,), np.uint8)
     lib().orc_nvfp4_quantize(_ptr(x), rows, D, g, _ptr(codes), _ptr(sc))
+    return codes, sc
+
+
+# --------------------------------------------------------------------------
+# Per-kv-head scales (compressed-tensors PR 436: "attn_head" strategy)
+# --------------------------------------------------------------------------
+
+def head_amax_bf16(x_bf16: np.ndarray) -> np.ndarray:
+    """x [rows][H][D] bf16 -> amax [H] (float32): max |x| over each kv head."""
+    x = _c(x_bf16, np.uint16)
+    rows, H, D = x.shape
+    out = np.empty(H, np.float32)
+    lib().orc_head_amax_bf16(_ptr(x), rows, H, D, _ptr(out))
+    return out
+
+
+def fp8_head_scales(x_bf16: np.ndarray) -> np.ndarray:
+    """Per-kv-head FP8 scales fl32(amax_h / 448) of x [rows][H][D]."""
+    return np.array([fp8_tensor_scale(float(a)) for a in head_amax_bf16(x_bf16)], np.float32)
+
+
+def nvfp4_head_scales(x_bf16: np.ndarray) -> np.ndarray:
+    """Per-kv-head NVFP4 global scales fl32(amax_h / 2688) of x [rows][H][D]."""
+    return np.array([nvfp4_global_scale(float(a)) for a in head_amax_bf16(x_bf16)], np.float32)
+
+
+def fp8_quantize_heads(x_bf16: np.ndarray, scales) -> np.ndarray:
+    """x [rows][H][D] -> codes, element [r][h][d] with scales[h]."""
+    x = _c(x_bf16, np.uint16)
+    rows, H, D = x.shape
+    sc = _c(scales, np.float32)
+    assert sc.size == H
+    out = np.empty(x.shape, np.uint8)
+    lib().orc_fp8_quantize_heads(_ptr(x), rows, H, D, _ptr(sc), _ptr(out))
+    return out
+
+
+def nvfp4_quantize_heads(x_bf16: np.ndarray, gs) -> tuple[np.ndarray, np.ndarray]:
+    """x [rows][H][D] -> (codes [rows][H][D/2], block scales [rows][H][D/16]),
+    head h with global scale gs[h]."""
+    x = _c(x_bf16, np.uint16)
+    rows, H, D = x.shape
+    g = _c(gs, np.float32)
+    assert g.size == H
+    codes = np.empty((rows, H, D // 2), np.uint8)
+    sc = np.empty((rows, H, D // 16), np.uint8)
+    lib().orc_nvfp4_quantize_heads(_ptr(x), rows, H, D, _ptr(g), _ptr(codes), _ptr(sc))
     return codes, sc
 
 

@@ -228,6 +228,41 @@ uint64_t orc_count_encode_mismatch(int kind, uint64_t first, uint64_t n,
   return total;
 }
 
+// Count, over the fp32 bit patterns [first, first + n) read as probabilities
+// p, the inputs whose code in `observed` differs from E4M3(fl32(p /
+// prob_scale)) -- the FP8-probability quantization step of
+// orc_attention_partial_probq ([VLLM-15734]: softmax(QK^T) quantized to FP8
+// with prob_output_scale).  Threaded.  Used to compare the device's division
+// by the prob scale with the oracle over every p in (0, 1].
+uint64_t orc_count_probq_mismatch(uint64_t first, uint64_t n, float prob_scale,
+                                  const uint8_t* observed, int nthreads,
+                                  uint64_t* first_bad_pattern) {
+  if (nthreads < 1) nthreads = 1;
+  std::vector<uint64_t> bad(nthreads, 0), firstbad(nthreads, UINT64_MAX);
+  std::vector<std::thread> th;
+  for (int t = 0; t < nthreads; ++t) {
+    th.emplace_back([&, t]() {
+      uint64_t lo = n * t / nthreads, hi = n * (t + 1) / nthreads;
+      for (uint64_t i = lo; i < hi; ++i) {
+        uint32_t bits = (uint32_t)(first + i);
+        float p;
+        std::memcpy(&p, &bits, 4);
+        if (std::isnan(p)) continue;
+        uint8_t want = e4m3_encode(fl32_div(p, prob_scale));
+        if (observed[i] != want) {
+          if (bad[t] == 0) firstbad[t] = first + i;
+          ++bad[t];
+        }
+      }
+    });
+  }
+  for (auto& x : th) x.join();
+  uint64_t total = 0, fb = UINT64_MAX;
+  for (int t = 0; t < nthreads; ++t) { total += bad[t]; fb = std::min(fb, firstbad[t]); }
+  if (first_bad_pattern) *first_bad_pattern = fb;
+  return total;
+}
+
 // Brute-force pin of the encoders: for every non-NaN fp32 pattern in
 // [first, first+n), pick the nearest grid value by a search over the sorted
 // table of decoded codes (ties to the code with an even mantissa, i.e. an
@@ -370,6 +405,60 @@ void orc_nvfp4_quantize(const uint16_t* x, size_t rows, int D, float g,
         cr[b * 8 + i] = (uint8_t)(nib[2 * i] | (nib[2 * i + 1] << 4));
     }
   }
+}
+
+// ===========================================================================
+// Per-kv-head static scales -- [CT-436] "Add support for 'attn_head' strategy"
+// (kv-cache recipe: num_bits 8, type float, symmetric, static_minmax observer,
+// strategy "attn_head"): one scale per attention head instead of one per
+// tensor.  For the KV cache the head is the kv head.  Reading used here: the
+// amax of kv head h runs over every token and dim of that head in the tensor
+// (K and V separately); its scale is the per-tensor formula applied to that
+// amax, and each element is quantized with its head's scale.
+//   x [rows][H][D] bf16 (rows = the tensor's tokens).
+// ===========================================================================
+
+// amax[h] = max |x[r][h][d]| over r and d.
+void orc_head_amax_bf16(const uint16_t* x, size_t rows, int H, int D, float* amax) {
+  for (int h = 0; h < H; ++h) {
+    double m = 0.0;
+    for (size_t r = 0; r < rows; ++r)
+      for (int d = 0; d < D; ++d) {
+        double v = std::fabs(bf16_value(x[(r * H + h) * (size_t)D + d]));
+        if (std::isnan(v)) die("head_amax: NaN input");
+        if (v > m) m = v;
+      }
+    amax[h] = (float)m;
+  }
+}
+
+// FP8: codes[r][h][d] = E4M3(fl32(x[r][h][d] / scales[h])).
+void orc_fp8_quantize_heads(const uint16_t* x, size_t rows, int H, int D,
+                            const float* scales, uint8_t* codes) {
+  for (size_t r = 0; r < rows; ++r)
+    for (int h = 0; h < H; ++h) {
+      const float s = scales[h];
+      if (!(s > 0.0f) || !std::isfinite(s)) die("fp8_quantize_heads: bad scale");
+      for (int d = 0; d < D; ++d) {
+        size_t i = (r * H + h) * (size_t)D + d;
+        codes[i] = e4m3_encode(fl32_div((float)bf16_value(x[i]), s));
+      }
+    }
+}
+
+// NVFP4 with a global scale per kv head: the block quantizer of
+// orc_nvfp4_quantize on each head's rows with g = gs[h].
+// codes [rows][H][D/2], bscales [rows][H][D/16].
+void orc_nvfp4_quantize(const uint16_t* x, size_t rows, int D, float g,
+                        uint8_t* codes, uint8_t* bscales);
+void orc_nvfp4_quantize_heads(const uint16_t* x, size_t rows, int H, int D,
+                              const float* gs, uint8_t* codes, uint8_t* bscales) {
+  for (size_t r = 0; r < rows; ++r)
+    for (int h = 0; h < H; ++h) {
+      size_t row = r * H + h;
+      orc_nvfp4_quantize(x + row * (size_t)D, 1, D, gs[h], codes + row * (size_t)(D / 2),
+                         bscales + row * (size_t)(D / 16));
+    }
 }
 
 // Dequantization (the fake-quant meaning of a stored code, [MO-714] "fake"):

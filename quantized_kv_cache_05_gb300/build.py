@@ -14,8 +14,10 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvq.so")
 SOURCES = ["kvq_api.cu", "kvq_append.cu", "kvq_decode.cu", "kvq_mla.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
-         "--expt-relaxed-constexpr"]
+# host code: no FP contraction (the host-side checks emulate device fp32
+# operations one by one)
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
+         "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"]
 
 
 def nvcc() -> str:

@@ -111,6 +111,61 @@ kvq_status check_params(const kvq_decode_params* p) {
 
 kvq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
+// ---------------------------------------------------------------------------
+// Division by the prob scale (FP8 probabilities, vLLM PR 15734: softmax(QK^T)
+// quantized to FP8 with prob_output_scale).  The kernels need E4M3(fl32(p /
+// y)) for p in [0, 1] and the call's y = prob_scale.  With z = RN(1/y), the
+// device's prob_quotient (q0 = RN(p z), r = RN(p - q0 y), q = RN(q0 + r z))
+// is within one fp32 step of RN(p/y) for every p, and equals it unless p/y
+// lies within about 2^-45 (relative) of the midpoint of two fp32 numbers.
+// Two adjacent fp32 numbers can round to different E4M3 codes only if one of
+// them is itself a rounding boundary of the E4M3 grid (a midpoint between two
+// E4M3 values: every such midpoint is an fp32 number).  So the codes of the
+// fast path equal those of the IEEE division for all p as soon as they do for
+// every p whose quotient lies within 1.5 fp32 steps of a boundary; the check
+// below runs the fast path on all p in a wider window (relative 2^-20) around
+// each boundary's preimage and requires the correctly rounded quotient there.
+// It is exact host arithmetic (this file is compiled with FP contraction off:
+// the product and the two fused multiply-adds are the device's operations).
+// ---------------------------------------------------------------------------
+
+float fast_quotient(float p, float y, float z) {
+  const float q0 = p * z;
+  const float r = std::fma(-q0, y, p);
+  return std::fma(r, z, q0);
+}
+
+// RN(p / y) in fp32: the double quotient is correctly rounded to 53 bits, and
+// rounding it to 24 bits gives the correctly rounded fp32 quotient (53 >= 2 *
+// 24 + 2).
+float exact_quotient(float p, float y) { return (float)((double)p / (double)y); }
+
+// Positive finite E4M3 values in increasing order (codes 0x00..0x7E).
+double e4m3_positive(int code) {
+  const int e = code >> 3, m = code & 7;
+  return e == 0 ? std::ldexp((double)m, -9) : std::ldexp(1.0 + m / 8.0, e - 7);
+}
+
+bool prob_reciprocal_ok(float y, float* z_out) {
+  if (!(y > 0.f) || !std::isfinite(y)) return false;
+  const float z = (float)(1.0 / (double)y);
+  if (!std::isfinite(z) || !(z > 0.f) || !std::isnormal(z)) return false;
+  for (int c = 0; c < 0x7E; ++c) {
+    const double mid = 0.5 * (e4m3_positive(c) + e4m3_positive(c + 1));   // a boundary
+    const double lo = mid * (1.0 - std::ldexp(1.0, -20)) * y;
+    const double hi = mid * (1.0 + std::ldexp(1.0, -20)) * y;
+    if (lo > 1.0) break;   // no p in (0, 1] reaches this boundary
+    float p = std::nextafter((float)lo, 0.f);
+    const float end = std::nextafter((float)std::min(hi, 1.0), 2.f);
+    for (; p <= end && p <= 1.f; p = std::nextafter(p, 2.f)) {
+      if (!std::isnormal(p)) continue;
+      if (fast_quotient(p, y, z) != exact_quotient(p, y)) return false;
+    }
+  }
+  *z_out = z;
+  return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -153,6 +208,16 @@ kvq_status kvq_encode_e2m1(const float* x, uint8_t* out, size_t n, void* stream)
   return cuda_status(launch_encode(1, x, out, n, as_stream(stream)));
 }
 
+kvq_status kvq_encode_prob_e4m3(const float* p, uint8_t* out, size_t n, float prob_scale,
+                                int* used_reciprocal, void* stream) {
+  if (!std::isfinite(prob_scale) || !(prob_scale > 0.f)) return KVQ_ERR_INVALID;
+  if (n > 0 && (!p || !out)) return KVQ_ERR_INVALID;
+  float z = 0.f;
+  const int fast = prob_reciprocal_ok(prob_scale, &z) ? 1 : 0;
+  if (used_reciprocal) *used_reciprocal = fast;
+  return cuda_status(launch_encode_prob(p, out, n, prob_scale, z, fast, as_stream(stream)));
+}
+
 kvq_status kvq_quantize_append(const kvq_cache* c, const void* k_new, const void* v_new,
                                const void* kpe_new, const int32_t* start_pos, int batch,
                                int n_tokens, void* stream) {
@@ -168,6 +233,8 @@ kvq_status kvq_quantize_append(const kvq_cache* c, const void* k_new, const void
     if (!v_new || !aligned16(v_new) || kpe_new) return KVQ_ERR_INVALID;
   }
   if ((long long)batch * n_tokens * c->num_kv_heads * c->head_dim >= (1LL << 40))
+    return KVQ_ERR_UNSUPPORTED;
+  if (batch > 32767 || c->num_kv_heads > 65535 || n_tokens >= (1 << 30))
     return KVQ_ERR_UNSUPPORTED;
   AppendArgs a{};
   a.fmt = c->fmt;
@@ -191,6 +258,10 @@ kvq_status kvq_quantize_append(const kvq_cache* c, const void* k_new, const void
   a.k_pe = static_cast<uint16_t*>(c->k_pe);
   a.k_scale = c->k_scale;
   a.v_scale = c->v_scale;
+  // RN(1/scale): the double quotient rounded to fp32 is the correctly rounded
+  // fp32 reciprocal (53 >= 2 * 24 + 2)
+  a.k_recip = (float)(1.0 / (double)c->k_scale);
+  a.v_recip = is_mla(c) ? a.k_recip : (float)(1.0 / (double)c->v_scale);
   a.has_v = is_mla(c) ? 0 : 1;
   return cuda_status(launch_append(a, as_stream(stream)));
 }
@@ -287,6 +358,7 @@ kvq_status decode_impl(const kvq_cache* c, const kvq_decode_params* p, const voi
   a.score_floats = (int)score_floats;
   a.qk_scale_log2 = p->sm_scale * c->k_scale * 1.4426950408889634f;
   a.prob_scale = p->prob_scale;
+  if (probq) a.prob_fast = prob_reciprocal_ok(p->prob_scale, &a.prob_recip) ? 1 : 0;
   a.fresh = p->fresh_tokens;
   a.counters = counters;
   a.out = out;
@@ -313,7 +385,7 @@ kvq_status decode_impl(const kvq_cache* c, const kvq_decode_params* p, const voi
   }
   if (p->qk_dim != D || p->v_dim != D) return KVQ_ERR_INVALID;
   const bool ok_dims = (c->fmt == KVQ_FP8_E4M3 && (D == 64 || D == 128)) ||
-                       (c->fmt == KVQ_NVFP4 && D == 128);
+                       (c->fmt == KVQ_NVFP4 && (D == 64 || D == 128 || D == 256));
   if (!ok_dims) return KVQ_ERR_UNSUPPORTED;
   a.out_mult = probq ? c->v_scale * p->prob_scale : c->v_scale;
   const uint64_t row_bytes = c->fmt == KVQ_FP8_E4M3 ? D : D / 2;
@@ -374,29 +446,23 @@ kvq_status kvq_decode_combine(const kvq_decode_params* p, const float* part_o,
 // serves them from one buffer the library itself carries: a file-scope device
 // array of KVQ_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds
 // until the process exits.  In host code the array's name is only a stand-in
-// for the symbol, so each device's real address is looked up once with
-// cudaGetSymbolAddress (with that device current) and passed to the kernel.
+// for the symbol, so the device's real address is looked up with
+// cudaGetSymbolAddress (with that device current) on every call and passed
+// to the kernel.
 // ---------------------------------------------------------------------------
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices] = {};
-
-// Device address of this device's scratch array (looked up on first use).
+// Device address of the scratch array on the current device.  Looked up on
+// every call: after the first call on a device (which loads the module) it is
+// a table lookup, and it stays right if the device's context is torn down
+// and created again (the module, and so the array, may then move).
 kvq_status noalloc_scratch(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return KVQ_ERR_CUDA;
-    g_noalloc_ptr[dev] = ptr;
-  }
-  *out = g_noalloc_ptr[dev];
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return KVQ_ERR_CUDA;
+  *out = ptr;
   return KVQ_OK;
 }
 

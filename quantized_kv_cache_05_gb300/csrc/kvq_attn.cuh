@@ -20,18 +20,23 @@ struct Geom {
   static constexpr int kBoxK = kBoxTokens * kRow;            // code bytes of one box
   static constexpr int kBoxS = kBoxTokens * kSRow;           // scale bytes of one box
   // one ring stage: [K codes][V codes][K scales][V scales], padded so that
-  // every stage starts on the 1024-byte swizzle period
-  static constexpr int kStage = (2 * (kBoxK + kBoxS) + 1023) / 1024 * 1024;
+  // every stage starts on the swizzle period (1024 bytes; 128 bytes for
+  // unswizzled 32-byte rows)
+  static constexpr int kAlign = kRow >= 64 ? 1024 : 128;
+  static constexpr int kStage = (2 * (kBoxK + kBoxS) + kAlign - 1) / kAlign * kAlign;
   static constexpr int kRing = kDecodeWarps * kStages * kStage;
   // FP8-probability mode streams K and V in separate sweeps: a stage holds
   // one box of one tensor, [codes][scales]
-  static constexpr int kStage1 = (kBoxK + kBoxS + 1023) / 1024 * 1024;
+  static constexpr int kStage1 = (kBoxK + kBoxS + kAlign - 1) / kAlign * kAlign;
   static constexpr int kKSteps = D / 16;   // QK k-steps over head_dim
   static constexpr int kMT = D / 16;       // PV m-tiles over v_dim
-  // physical 16-byte chunk of logical chunk `ch` in row `row` of a box
+  static_assert(kRow == 32 || kRow == 64 || kRow == 128, "code rows of 32, 64 or 128 bytes");
+  // physical 16-byte chunk of logical chunk `ch` in row `row` of a box (the
+  // TMA swizzle of the row width: 128-byte, 64-byte, none for 32 bytes)
   __device__ static __forceinline__ int swz(int row, int ch) {
     if constexpr (kRow == 128) return ch ^ (row & 7);
-    else return ch ^ ((row >> 1) & 3);                        // 64-byte rows
+    else if constexpr (kRow == 64) return ch ^ ((row >> 1) & 3);
+    else return ch;
   }
 };
 
@@ -68,17 +73,46 @@ __device__ __forceinline__ void k_frag(uint32_t boxK, uint32_t boxKs, int row, i
       e4m3x4_to_f16x2x2(v.w, b[i * 4 + 3][0], b[i * 4 + 3][1]);
     }
   } else {
-    static_assert(D == 128, "NVFP4 decode supports head_dim 128");
-    uint4 v = lds128(boxK + row * Gm::kRow + (Gm::swz(row, t) << 4));
-    uint32_t sc = lds16(boxKs + row * SSTRIDE + 2 * t);   // blocks 2t, 2t+1
-    uint32_t s2 = e4m3x2_to_f16x2(sc);
-    uint32_t s_lo = __byte_perm(s2, 0, 0x1010), s_hi = __byte_perm(s2, 0, 0x3232);
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    // NVFP4: the lane's D/4 dims are D/8 code bytes (D/32 words) and D/64
+    // blocks; word k is scaled by block k/2 of the lane's range
+    constexpr int NWK = D / 32;
+    uint32_t w[NWK];
+    if constexpr (D == 64) {
+      const uint2 v = lds64(boxK + row * Gm::kRow + 8 * t);
+      w[0] = v.x; w[1] = v.y;
+    } else if constexpr (D == 128) {
+      const uint4 v = lds128(boxK + row * Gm::kRow + (Gm::swz(row, t) << 4));
+      w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else {
+      static_assert(D == 256, "NVFP4 decode supports head_dim 64, 128 and 256");
+      const uint4 v0 = lds128(boxK + row * Gm::kRow + (Gm::swz(row, 2 * t) << 4));
+      const uint4 v1 = lds128(boxK + row * Gm::kRow + (Gm::swz(row, 2 * t + 1) << 4));
+      w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+      w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+    }
+    // f16 block scales, each duplicated into both halves
+    constexpr int NB = (NWK + 1) / 2;
+    uint32_t sc[NB];
+    if constexpr (D == 64) {
+      const uint32_t s2 = e4m3x2_to_f16x2(lds8(boxKs + row * SSTRIDE + t));
+      sc[0] = __byte_perm(s2, 0, 0x1010);
+    } else if constexpr (D == 128) {
+      const uint32_t s2 = e4m3x2_to_f16x2(lds16(boxKs + row * SSTRIDE + 2 * t));
+      sc[0] = __byte_perm(s2, 0, 0x1010);
+      sc[1] = __byte_perm(s2, 0, 0x3232);
+    } else {
+      const uint32_t s4 = lds32(boxKs + row * SSTRIDE + 4 * t);
+      const uint32_t sa = e4m3x2_to_f16x2(s4 & 0xFFFFu), sb = e4m3x2_to_f16x2(s4 >> 16);
+      sc[0] = __byte_perm(sa, 0, 0x1010);
+      sc[1] = __byte_perm(sa, 0, 0x3232);
+      sc[2] = __byte_perm(sb, 0, 0x1010);
+      sc[3] = __byte_perm(sb, 0, 0x3232);
+    }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < NWK; ++k) {
       uint32_t o0, o1, o2, o3;
       e2m1x8_to_f16x2x4(w[k], o0, o1, o2, o3);
-      uint32_t s = k < 2 ? s_lo : s_hi;
+      const uint32_t s = sc[k >> 1];
       b[2 * k][0] = hmul2(o0, s);
       b[2 * k][1] = hmul2(o1, s);
       b[2 * k + 1][0] = hmul2(o2, s);
@@ -128,25 +162,47 @@ __device__ __forceinline__ void v_frag(uint32_t boxV, uint32_t boxVs, int t, int
       e4m3x4_to_f16x2x2(q1, a[2 * k + 1][2], a[2 * k + 1][3]);
     }
   } else {
-    static_assert(FMT == kFmtNvfp4 && D == 128, "unsupported V layout");
-    // 16 elements per token: bytes [8g, 8g+8) of the 64-byte row, block g
-    uint2 v[4];
-    uint32_t sc[4];
+    // NVFP4: lane g's value dims (D/8) g .. are D/16 code bytes per token
+    // (NW words) in D/128 blocks (one for D <= 128); word k is scaled by
+    // block k/2 of the lane's range
+    constexpr int NW = D / 64;
+    constexpr int NB = (NW + 1) / 2;
+    uint32_t v[4][NW];
+    uint32_t sc[4][NB];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      v[r] = lds64(boxV + tk[r] * 64 + (Gm::swz(tk[r], g >> 1) << 4) + ((g & 1) << 3));
-      sc[r] = lds8(boxVs + tk[r] * SSTRIDE + g);
+      if constexpr (D == 64) {
+        v[r][0] = lds32(boxV + tk[r] * Gm::kRow + 4 * g);
+        sc[r][0] = lds8(boxVs + tk[r] * SSTRIDE + (g >> 1));
+      } else if constexpr (D == 128) {
+        const uint2 x = lds64(boxV + tk[r] * Gm::kRow + (Gm::swz(tk[r], g >> 1) << 4) +
+                              ((g & 1) << 3));
+        v[r][0] = x.x; v[r][1] = x.y;
+        sc[r][0] = lds8(boxVs + tk[r] * SSTRIDE + g);
+      } else {
+        static_assert(FMT == kFmtNvfp4 && D == 256, "unsupported V layout");
+        const uint4 x = lds128(boxV + tk[r] * Gm::kRow + (Gm::swz(tk[r], g) << 4));
+        v[r][0] = x.x; v[r][1] = x.y; v[r][2] = x.z; v[r][3] = x.w;
+        const uint32_t s2 = lds16(boxVs + tk[r] * SSTRIDE + 2 * g);
+        sc[r][0] = s2 & 0xFFu;
+        sc[r][1] = s2 >> 8;
+      }
       if (tk[r] >= nvalid) {
-        v[r] = make_uint2(0, 0);
-        sc[r] = 0;
+#pragma unroll
+        for (int k = 0; k < NW; ++k) v[r][k] = 0u;
+#pragma unroll
+        for (int k = 0; k < NB; ++k) sc[r][k] = 0u;
       }
     }
-    const uint32_t s01 = e4m3x2_to_f16x2(sc[0] | (sc[1] << 8));   // (scale_2t, scale_2t+1)
-    const uint32_t s89 = e4m3x2_to_f16x2(sc[2] | (sc[3] << 8));
+    uint32_t s01[NB], s89[NB];   // (scale of token 2t, 2t+1) and (2t+8, 2t+9)
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const uint32_t A = k ? v[0].y : v[0].x, B = k ? v[1].y : v[1].x;
-      const uint32_t C = k ? v[2].y : v[2].x, E = k ? v[3].y : v[3].x;
+    for (int k = 0; k < NB; ++k) {
+      s01[k] = e4m3x2_to_f16x2(sc[0][k] | (sc[1][k] << 8));
+      s89[k] = e4m3x2_to_f16x2(sc[2][k] | (sc[3][k] << 8));
+    }
+#pragma unroll
+    for (int k = 0; k < NW; ++k) {
+      const uint32_t A = v[0][k], B = v[1][k], C = v[2][k], E = v[3][k];
       const uint32_t evAB = (A & 0x0F0F0F0Fu) | ((B & 0x0F0F0F0Fu) << 4);
       const uint32_t odAB = ((A >> 4) & 0x0F0F0F0Fu) | (B & 0xF0F0F0F0u);
       const uint32_t evCE = (C & 0x0F0F0F0Fu) | ((E & 0x0F0F0F0Fu) << 4);
@@ -156,13 +212,14 @@ __device__ __forceinline__ void v_frag(uint32_t boxV, uint32_t boxVs, int t, int
       e2m1x8_to_f16x2x4(odAB, o[0], o[1], o[2], o[3]);
       e2m1x8_to_f16x2x4(evCE, f[0], f[1], f[2], f[3]);
       e2m1x8_to_f16x2x4(odCE, h[0], h[1], h[2], h[3]);
+      const uint32_t sa = s01[k >> 1], sb = s89[k >> 1];
 #pragma unroll
       for (int bb = 0; bb < 4; ++bb) {
         const int i = 4 * k + bb;   // value dims (D/8) g + 8k + 2bb (+1)
-        a[i][0] = hmul2(e[bb], s01);
-        a[i][1] = hmul2(o[bb], s01);
-        a[i][2] = hmul2(f[bb], s89);
-        a[i][3] = hmul2(h[bb], s89);
+        a[i][0] = hmul2(e[bb], sa);
+        a[i][1] = hmul2(o[bb], sa);
+        a[i][2] = hmul2(f[bb], sb);
+        a[i][3] = hmul2(h[bb], sb);
       }
     }
   }

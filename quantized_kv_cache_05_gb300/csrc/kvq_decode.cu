@@ -74,15 +74,17 @@ struct Ring {
 
 // Resident CTAs per SM the kernel is compiled for: four for the half-size
 // ring of the FP8-probability mode with up to eight query heads per kv head,
-// three otherwise, two with sixteen heads (twice the accumulators).
-template <int FMT, bool PROBQ, int NH>
+// three otherwise, two with sixteen heads (twice the accumulators); head_dim
+// 256 has twice the fragments and ring of 128: two, one with sixteen heads.
+template <int FMT, int D, bool PROBQ, int NH>
 constexpr int ctas_per_sm() {
+  if (D >= 256) return NH == 2 ? 1 : 2;
   return NH == 2 ? 2 : PROBQ ? 4 : 3;
 }
 
 // NH = number of 8-head groups (1: up to 8 query heads per kv head, 2: up to 16)
 template <int FMT, int D, bool PROBQ, int NH>
-__global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, PROBQ, NH>())
+__global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>())
     partial_kernel(const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PartialArgs a) {
   using Gm = Geom<FMT, D>;
@@ -201,24 +203,47 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, PROBQ, NH>())
   };
 
   int issued = 0;
-  if (lane == 0)
+  if (lane == 0) {
+#pragma unroll 1   // one copy of the issue code (it runs cold, once per CTA)
     for (; issued < min(total, kStages); ++issued) issue(issued);
+  }
 
   const int hq0 = h * a.G;
   // Q^T fragments (B operand of S^T = K Q^T: k = head dims, n = query heads
-  // g + 8 hh), head dims permuted like the K fragments
+  // g + 8 hh), head dims permuted like the K fragments.  Each head is scaled
+  // by its power of two 2^e (q_prescale_exp) before the f16 conversion, so
+  // the bf16 query keeps its full range; qsc[hh][e] is the score scale
+  // (sm_scale * k_scale * log2 e * 2^-e) of head 2t + e + 8hh, the head of
+  // this lane's accumulator columns.
   uint32_t qb[KS][NH][2];
+  float qsc[NH][2];
 #pragma unroll
   for (int hh = 0; hh < NH; ++hh) {
     const int head = g + 8 * hh;
     const bool valid = head < a.G;
     const uint16_t* qp = a.q + ((size_t)b * a.Hq + hq0 + (valid ? head : 0)) * D + (D / 4) * t;
+    uint2 raw[KS];
+    uint32_t mx2 = 0;   // two packed 16-bit maxima of |q|
 #pragma unroll
     for (int j = 0; j < KS; ++j) {
-      uint2 v = valid ? *reinterpret_cast<const uint2*>(qp + 4 * j) : make_uint2(0, 0);
-      qb[j][hh][0] = pack_f16x2(bf16_bits_to_f32(v.x & 0xFFFFu), bf16_bits_to_f32(v.x >> 16));
-      qb[j][hh][1] = pack_f16x2(bf16_bits_to_f32(v.y & 0xFFFFu), bf16_bits_to_f32(v.y >> 16));
+      raw[j] = valid ? *reinterpret_cast<const uint2*>(qp + 4 * j) : make_uint2(0, 0);
+      mx2 = __vmaxu2(mx2, __vmaxu2(raw[j].x & 0x7FFF7FFFu, raw[j].y & 0x7FFF7FFFu));
     }
+    // the head's D elements sit in the four lanes t = 0..3 of row g
+    uint32_t mx = max(mx2 & 0xFFFFu, mx2 >> 16);
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const int e = q_prescale_exp(mx);
+    const float f = exp2i(e);
+#pragma unroll
+    for (int j = 0; j < KS; ++j) {
+      const uint2 v = raw[j];
+      qb[j][hh][0] = pack_f16x2(__uint_as_float(v.x << 16) * f, __uint_as_float(v.x & 0xFFFF0000u) * f);
+      qb[j][hh][1] = pack_f16x2(__uint_as_float(v.y << 16) * f, __uint_as_float(v.y & 0xFFFF0000u) * f);
+    }
+    const float my = scale_pow2(a.qk_scale_log2, -e);   // head g + 8hh
+    qsc[hh][0] = __shfl_sync(0xffffffffu, my, 4 * (2 * t));
+    qsc[hh][1] = __shfl_sync(0xffffffffu, my, 4 * (2 * t + 1));
   }
 
   // O^T accumulators: m-tile i (value dims), head group hh; C layout
@@ -275,7 +300,7 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, PROBQ, NH>())
                     qb[kk + 1][hh][0], qb[kk + 1][hh][1]);
           }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) x[hh][e] = (s0[e] + s1[e]) * a.qk_scale_log2;
+          for (int e = 0; e < 4; ++e) x[hh][e] = (s0[e] + s1[e]) * qsc[hh][e & 1];
           if (nvalid < kBoxTokens) {   // ragged tail of the chunk
 #pragma unroll
             for (int e = 0; e < 4; ++e)
@@ -326,11 +351,12 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, PROBQ, NH>())
             }
             l[hh][0] += p[0] + p[2];
             l[hh][1] += p[1] + p[3];
-            const float ps = a.prob_scale;
-            const uint32_t c01 =
-                e4m3x2_to_f16x2(f32x2_to_e4m3x2(__fdiv_rn(p[0], ps), __fdiv_rn(p[1], ps)));
-            const uint32_t c23 =
-                e4m3x2_to_f16x2(f32x2_to_e4m3x2(__fdiv_rn(p[2], ps), __fdiv_rn(p[3], ps)));
+            const float ps = a.prob_scale, pz = a.prob_recip;
+            const bool fast = a.prob_fast != 0;
+            const uint32_t c01 = e4m3x2_to_f16x2(f32x2_to_e4m3x2(
+                prob_quotient(p[0], ps, pz, fast), prob_quotient(p[1], ps, pz, fast)));
+            const uint32_t c23 = e4m3x2_to_f16x2(f32x2_to_e4m3x2(
+                prob_quotient(p[2], ps, pz, fast), prob_quotient(p[3], ps, pz, fast)));
             pb[hh][0] = movmatrix_trans(c01);   // (tokens 2t, 2t+1; head g)
             pb[hh][1] = movmatrix_trans(c23);   // (tokens 2t+8, 2t+9; head g)
           }
@@ -521,7 +547,7 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, PROBQ, NH>())
   // fragments are written out), the weights at the ring end
   if (a.counters) {
     constexpr uint32_t kWbuf = (kMaxGroup * kMaxFusedSplits + kMaxGroup) * 4;
-    fused_combine_staged<ctas_per_sm<FMT, PROBQ, NH>() == 4 ? 16 : 32>(
+    fused_combine_staged<ctas_per_sm<FMT, D, PROBQ, NH>() == 4 ? 16 : 32>(
         a, bh, part_row, a.G, ring, reinterpret_cast<const float*>(ofrag), Rg::kBytes - kWbuf,
         reinterpret_cast<float*>(dyn_smem + (ring - smem_u32(dyn_smem)) + Rg::kBytes - kWbuf),
         smem_u32(&sm.comb_full));
@@ -575,6 +601,8 @@ cudaError_t launch_partial(int fmt, int D, bool probq, const TensorMaps& m, cons
   if (fmt == kFmtFp8 && D == 128) return dispatch_nh<kFmtFp8, 128>(probq, m, a, st);
   if (fmt == kFmtFp8 && D == 64) return dispatch_nh<kFmtFp8, 64>(probq, m, a, st);
   if (fmt == kFmtNvfp4 && D == 128) return dispatch_nh<kFmtNvfp4, 128>(probq, m, a, st);
+  if (fmt == kFmtNvfp4 && D == 64) return dispatch_nh<kFmtNvfp4, 64>(probq, m, a, st);
+  if (fmt == kFmtNvfp4 && D == 256) return dispatch_nh<kFmtNvfp4, 256>(probq, m, a, st);
   return cudaErrorInvalidValue;
 }
 

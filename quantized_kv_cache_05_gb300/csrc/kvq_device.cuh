@@ -89,6 +89,32 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
 // bf16 bits -> fp32 (exact)
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
+// 2^n as an fp32, for -126 <= n <= 127 (a normal number: exact).
+__device__ __forceinline__ float exp2i(int n) { return __uint_as_float((uint32_t)(n + 127) << 23); }
+
+// Power-of-two prescale of a bf16 query head for the f16 tensor-core
+// operand.  `bits` is the head's largest |q| as bf16 magnitude bits.  The
+// result e puts that element into [2^14, 2^15) (0 for an all-zero head; at
+// most 127, reached only when the largest |q| is below 2^-113): every element
+// of the head within 2^-31 of its largest then converts to f16 exactly (bf16
+// keeps 8 significant bits, f16 11 down to 2^-14 and 8 down to 2^-17), and
+// smaller ones are rounded at the f16 subnormal step, at most 2^-40 of the
+// head's largest |q| -- whatever q's magnitude.  x * 2^e is one exact fp32
+// product (e in [-113, 127]); the score scale takes 2^-e.
+__device__ __forceinline__ int q_prescale_exp(uint32_t bits) {
+  if (bits == 0) return 0;
+  const int E = (int)(bits >> 7);
+  const int lg = E > 0 ? E - 127 : (31 - __clz((int)bits)) - 133;   // floor(log2 |q|max)
+  return min(14 - lg, 127);
+}
+
+// x * 2^e for e in [-252, 254], as two exact power-of-two products (only a
+// result below the fp32 normal range is rounded).
+__device__ __forceinline__ float scale_pow2(float x, int e) {
+  const int e1 = e >> 1;
+  return (x * exp2i(e1)) * exp2i(e - e1);
+}
+
 // ---------------------------------------------------------------------------
 // Warp-level tensor-core MMA: D(16x8,f32) += A(16x16) * B(16x8)
 // Fragment layout (g = lane >> 2, t = lane & 3):
@@ -255,6 +281,26 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 // Lets the next (programmatically serialized) kernel in the stream launch.
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// fl32(p / y) for the FP8 probabilities, with y = prob_scale known per call.
+// fast: z = RN(1/y) precomputed; q0 = RN(p z) has a relative error of at most
+// about 2^-23, the remainder r = RN(p - q0 y) is then accurate to 2^-24, and
+// RN(q0 + r z) = RN(p/y + h) with |h| below 2^-45 (p/y).  The result is the
+// correctly rounded quotient except where p/y lies that close to the midpoint
+// of two fp32 numbers, and is always within one fp32 step of it (the
+// correction step of P. Markstein, "Computation of elementary functions on the
+// IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990; division by
+// a divisor known in advance: N. Brisebarre, J.-M. Muller, S. K. Raina, IEEE
+// Trans. Computers 53(8), 2004).  The host enables it for a prob_scale only
+// after checking that it returns the correctly rounded quotient for every p
+// whose quotient lies near an E4M3 rounding boundary, so that the E4M3 codes
+// equal those of the IEEE division for all p; otherwise the IEEE division.
+__device__ __forceinline__ float prob_quotient(float p, float y, float z, bool fast) {
+  if (!fast) return __fdiv_rn(p, y);
+  const float q0 = __fmul_rn(p, z);
+  const float r = __fmaf_rn(-q0, y, p);
+  return __fmaf_rn(r, z, q0);
 }
 
 __device__ __forceinline__ void record_error(int32_t* flag, int bits) {

@@ -36,6 +36,7 @@ struct AppendArgs {
   uint8_t* v_bscale;
   uint16_t* k_pe;
   float k_scale, v_scale;
+  float k_recip, v_recip;     // RN(1 / scale) of the FP8 scales
   int has_v;
 };
 
@@ -56,6 +57,8 @@ struct PartialArgs {
   float pe_scale_log2;        // MLA rope part: sm_scale * log2(e)
   float out_mult;             // v_scale (times prob_scale with FP8 probabilities)
   float prob_scale;           // > 0: FP8 probabilities
+  float prob_recip;           // RN(1 / prob_scale), used when prob_fast
+  int prob_fast;              // 1: p / prob_scale by the reciprocal and one correction
   int fresh;                  // > 0: only the last `fresh` positions wait for the append
   // fused combine (kvq_decode): arrival counters [B * Hkv] and the output
   uint32_t* counters;         // null: partials only
@@ -93,6 +96,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_amax_bf16(const uint16_t* x, size_t n, float* out, cudaStream_t st);
 cudaError_t launch_encode(int kind, const float* x, uint8_t* out, size_t n, cudaStream_t st);
+// E4M3(fl32(p / prob_scale)) per element, through the decode kernel's division
+cudaError_t launch_encode_prob(const float* p, uint8_t* out, size_t n, float prob_scale,
+                               float prob_recip, int prob_fast, cudaStream_t st);
 // TMA descriptors of the K and V code tensors (16-row boxes).
 struct TensorMaps {
   CUtensorMap k16, v16;

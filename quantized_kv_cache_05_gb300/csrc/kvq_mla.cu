@@ -100,6 +100,8 @@ struct MlaSmem {
   float wmax[2][kMlaHeads];        // per-warp tile maxima
   float lsum[2][kMlaHeads];        // per-warp denominators (end)
   float m[kMlaHeads];              // final reference max (end)
+  uint32_t qmax[kMlaHeads];        // largest |q_lat| per head (bf16 magnitude bits)
+  float qfac[kMlaHeads];           // latent score scale per head (log2 domain)
   int pages[kPageCache];
 };
 
@@ -221,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm.comb_full), 1);
     sm.abort_flag = 0;
     sm.rescale[0] = sm.rescale[1] = 0;
+    for (int h = 0; h < kMlaHeads; ++h) sm.qmax[h] = 0u;
     fence_barrier_init();
     prefetch_tmap(&tmCodes);
     prefetch_tmap(&tmPe);
@@ -426,6 +429,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           qv[k] = *reinterpret_cast<const uint4*>(qg + (size_t)(i / (kMlaQkDim / 8)) * kMlaQkDim +
                                                   (i % (kMlaQkDim / 8)) * 8);
       }
+      // The latent part of each head is scaled by its power of two 2^e
+      // (q_prescale_exp of the head's largest |q_lat|) before the f16
+      // conversion, so that the bf16 query keeps its full range; 2^-e goes
+      // into the head's score scale.  The rope part stays bf16 (exact).
+#pragma unroll
+      for (int k = 0; k < kQPer; ++k) {
+        const int i = dt + k * kDecoders;
+        if (i >= kQItems) break;
+        const int h = i / (kMlaQkDim / 8), d = (i % (kMlaQkDim / 8)) * 8;
+        if (d < kMlaLat) {
+          const uint4 v = qv[k];
+          const uint32_t m2 = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                       __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+          const uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
+          if (mx) atomicMax(&sm.qmax[h], mx);
+        }
+      }
+      asm volatile("bar.sync 3, %0;" ::"n"(kDecoders) : "memory");   // decode warps only
 #pragma unroll
       for (int k = 0; k < kQPer; ++k) {
         const int i = dt + k * kDecoders;
@@ -433,16 +454,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = i / (kMlaQkDim / 8), d = (i % (kMlaQkDim / 8)) * 8;
         const uint4 v = qv[k];
         if (d < kMlaLat) {
+          const float fs = exp2i(q_prescale_exp(sm.qmax[h]));
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
           uint32_t f[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            f[j] = pack_f16x2(bf16_bits_to_f32(w[j] & 0xFFFFu), bf16_bits_to_f32(w[j] >> 16));
+            f[j] = pack_f16x2(__uint_as_float(w[j] << 16) * fs,
+                              __uint_as_float(w[j] & 0xFFFF0000u) * fs);
           sts128(base + kOffQLat + (d >> 6) * 2048 + swz(h, d & 63), f[0], f[1], f[2], f[3]);
         } else {
           sts128(base + kOffQPe + swz(h, d - kMlaLat), v.x, v.y, v.z, v.w);
         }
       }
+      if (dt < kMlaHeads) sm.qfac[dt] = scale_pow2(a.qk_scale_log2, -q_prescale_exp(sm.qmax[dt]));
+      // the softmax warps read the score scales after this barrier
+      asm volatile("bar.arrive 2, %0;" ::"n"(kDecoders + 64) : "memory");
     }
     // Decode of tile x into tile buffer x % 2 (decode warps).  A unit is
     // (token, 64-dim column, half) = 32 dims; eight consecutive threads take
@@ -558,6 +584,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       // ---- softmax warps: tile t, one token per thread, all 16 heads
+      asm volatile("bar.sync 2, %0;" ::"n"(kDecoders + 64) : "memory");   // score scales written
+      float qf[kMlaHeads];
+#pragma unroll
+      for (int h = 0; h < kMlaHeads; ++h) qf[h] = sm.qfac[h];
       int nresc = 0;
       for (int t = 0; t < nt; ++t) {
         wait_bar(smem_u32(&sm.s_done[t & 1]), (t >> 1) & 1, abort_flag);
@@ -573,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool need = false;
 #pragma unroll
         for (int h = 0; h < kMlaHeads; ++h) {
-          xs[h] = valid ? __uint_as_float(sl[h]) * a.qk_scale_log2 +
+          xs[h] = valid ? __uint_as_float(sl[h]) * qf[h] +
                               __uint_as_float(sp[h]) * a.pe_scale_log2
                         : -INFINITY;
           need |= xs[h] > m[h] + kLazyMax;

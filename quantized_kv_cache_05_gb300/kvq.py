@@ -67,6 +67,7 @@ SIGNATURES = {
                                   _P, _P, _P]),
     "kvq_encode_e4m3": (_int, [_P, _P, _sz, _P]),
     "kvq_encode_e2m1": (_int, [_P, _P, _sz, _P]),
+    "kvq_encode_prob_e4m3": (_int, [_P, _P, _sz, _f, ctypes.POINTER(_int), _P]),
 }
 
 _lock = threading.Lock()
@@ -194,3 +195,12 @@ def kvq_encode_e4m3(x, out, n: int, stream=None) -> int:
 
 def kvq_encode_e2m1(x, out, n: int, stream=None) -> int:
     return lib().kvq_encode_e2m1(_addr(x), _addr(out), n, _stream(stream))
+
+
+def kvq_encode_prob_e4m3(p, out, n: int, prob_scale: float, stream=None) -> tuple[int, int]:
+    """E4M3 codes of fl32(p / prob_scale) as the decode kernels compute them;
+    returns (status, 1 if the reciprocal path was used else 0)."""
+    used = _int(0)
+    st = lib().kvq_encode_prob_e4m3(_addr(p), _addr(out), n, prob_scale, ctypes.byref(used),
+                                    _stream(stream))
+    return st, int(used.value)

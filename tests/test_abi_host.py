@@ -6,6 +6,7 @@ import math
 import os
 import re
 
+import numpy as np
 import pytest
 
 from conftest import ROOT
@@ -44,7 +45,9 @@ def test_tensor_scale():
     assert kvq.kvq_tensor_scale(kvq.KVQ_NVFP4, 2688.0) == (0, 1.0)
     assert kvq.kvq_tensor_scale(kvq.KVQ_FP8_E4M3, 0.0) == (0, 1.0)
     st, s = kvq.kvq_tensor_scale(kvq.KVQ_FP8_E4M3, 7.53125)
-    assert st == 0 and s == float(ctypes.c_float(7.53125 / 448.0).value) or s > 0
+    assert st == 0
+    # one IEEE fp32 division: 7.53125 / 448 rounded once to float
+    assert s == float(np.float32(np.float32(7.53125) / np.float32(448.0)))
     for bad in [-1.0, math.nan, math.inf]:
         assert kvq.kvq_tensor_scale(kvq.KVQ_FP8_E4M3, bad)[0] == kvq.KVQ_ERR_INVALID
     assert kvq.kvq_tensor_scale(7, 1.0)[0] == kvq.KVQ_ERR_INVALID
@@ -216,3 +219,35 @@ def test_fused_decode_rejects(L):
     assert kvq.kvq_decode_combine(p, 0x60000, 0x70000, 0x80000, None) == kvq.KVQ_ERR_UNSUPPORTED
     p.num_splits, p.batch = 2, 0
     assert f(c, p, None, None, None, None, None, None) == kvq.KVQ_OK
+
+
+def test_prob_division_host_check():
+    """n = 0 runs only the host check of the FP8-probability division: the
+    reciprocal path is accepted for the workloads' prob scale fl32(1/448)
+    and for other scales; invalid scales are refused."""
+    import numpy as np
+    for ps in [np.float32(1 / 448), np.float32(1 / 240), np.float32(0.00311), 2.0 ** -8]:
+        assert kvq.kvq_encode_prob_e4m3(None, None, 0, float(ps)) == (kvq.KVQ_OK, 1)
+    for bad in [0.0, -1.0, math.inf, math.nan]:
+        assert kvq.kvq_encode_prob_e4m3(None, None, 0, bad)[0] == kvq.KVQ_ERR_INVALID
+
+
+def nvfp4_cache(D):
+    c = good_cache()
+    c.fmt, c.head_dim = kvq.KVQ_NVFP4, D
+    c.k_bscale, c.v_bscale = 0xA0000, 0xB0000
+    return c
+
+
+@pytest.mark.parametrize("D,want", [(40, kvq.KVQ_ERR_INVALID),        # D % 16 != 0
+                                    (24, kvq.KVQ_ERR_INVALID),
+                                    (96, kvq.KVQ_ERR_UNSUPPORTED),    # valid, no kernel
+                                    (512, kvq.KVQ_ERR_UNSUPPORTED)])  # only as the MLA latent
+def test_nvfp4_head_dims_refused_before_launch(L, D, want):
+    """NVFP4 decode runs at head_dim 64, 128 and 256; a cache whose head_dim
+    is not a multiple of 16 is invalid, other multiples are refused as
+    unsupported -- in both cases before any launch."""
+    c, p = nvfp4_cache(D), good_params()
+    p.qk_dim = p.v_dim = D
+    assert kvq.kvq_decode_partial(c, p, 0x50000, 0x60000, 0x70000, None) == want
+    assert kvq.kvq_decode(c, p, 0x50000, 0x60000, 0x70000, 0x90000, 0x80000, None) == want

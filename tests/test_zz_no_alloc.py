@@ -5,8 +5,10 @@ belongs to a host framework's fixed pool, or a memory budget forbids another
 cudaMalloc.  kvq_decode_noalloc keeps the split partials and arrival counters
 in the library's own static device buffer (4 MiB).  These tests call it
 through the C ABI twice in a row and compare each result with kvq_decode
-(caller-owned buffers) within the fp32 tolerance the other tests use, and
-check that requests larger than the buffer are refused.  This file is
+(caller-owned buffers) within the fp32 tolerance the other tests use; check
+a request that fills the buffer exactly and refuse the next larger one; and
+run it right after an append with fresh_tokens = 1 (accepted; the decode
+then simply starts after the append).  This file is
 collected last so that a run stopping at the first failure has already run
 everything else; it also passes on its own in a fresh process.
 """
@@ -16,7 +18,7 @@ import numpy as np
 import pytest
 import torch
 
-from kvq_testlib import Setup, assert_f32_close
+from kvq_testlib import Setup, assert_f32_close, to_dev_bf16
 from quantized_kv_cache_05_gb300 import build as kbuild
 from quantized_kv_cache_05_gb300 import kvq, runtime, synth
 
@@ -70,3 +72,57 @@ def test_noalloc_refuses_requests_beyond_its_buffer():
     need = 4 * 32 * 64 * (128 + 1) * 4
     assert need > kvq.KVQ_NOALLOC_SCRATCH_BYTES
     assert kvq.kvq_decode_noalloc(S.cache.struct(), p, S.q_t, out) == kvq.KVQ_ERR_WORKSPACE
+
+
+def _exact_fit_workload():
+    """64 requests x 4 kv heads (MHA, head_dim 64), 63 splits: counters
+    1 KiB + partial lse 63 KiB + partial o 4032 KiB = exactly 4 MiB."""
+    w = synth.Workload("noalloc_fit", "fp8", 64, 4, 4, 64, np.full(64, 1008, np.int32))
+    rows = w.B * w.Hq * 63
+    need = 4 * w.B * w.Hkv + 4 * rows + 4 * rows * w.Dv
+    assert need == kvq.KVQ_NOALLOC_SCRATCH_BYTES
+    return w
+
+
+def test_noalloc_exact_fit_and_one_more_request():
+    w = _exact_fit_workload()
+    S = Setup(w)
+    cfg = S.config(63, "f32")
+    ref = runtime.decode_fused(S.cache, S.q_t, S.seq_lens_t, cfg).clone()
+    torch.cuda.synchronize()
+    out = torch.full_like(ref, math.nan)
+    p = cfg.params(S.seq_lens_t)
+    assert kvq.kvq_decode_noalloc(S.cache.struct(), p, S.q_t, out) == kvq.KVQ_OK
+    torch.cuda.synchronize()
+    assert_f32_close(out.cpu().numpy(), ref.cpu().numpy().astype(np.float64), "exact fit")
+    # one more request needs 4 B of counters and 63 rows of partials more
+    p.batch = w.B + 1
+    assert kvq.kvq_decode_noalloc(S.cache.struct(), p, S.q_t, out) == kvq.KVQ_ERR_WORKSPACE
+
+
+def test_noalloc_after_append_with_fresh_tokens():
+    """Append each request's last row (other values first, then the true
+    row), then kvq_decode_noalloc with fresh_tokens = 1 on the same stream:
+    the result equals kvq_decode's on the true cache."""
+    w = synth.gqa_fp8(700)
+    w.B, w.Hq, w.Hkv = 2, 8, 2
+    w.seq_lens = np.array([700, 129], np.int32)
+    S = Setup(w)
+    cfg = S.config(3, "f32")
+    ref = runtime.decode_fused(S.cache, S.q_t, S.seq_lens_t, cfg).clone()
+    torch.cuda.synchronize()
+    last = [int(L) - 1 for L in w.seq_lens]
+    k_last = to_dev_bf16(np.stack([S.k[b][last[b]:last[b] + 1] for b in range(w.B)]))
+    v_last = to_dev_bf16(np.stack([S.v[b][last[b]:last[b] + 1] for b in range(w.B)]))
+    start = torch.tensor(last, dtype=torch.int32, device="cuda")
+    c = S.cache.struct()
+    # stale rows (sign-flipped) first, so that reading before the append shows
+    kvq.check(kvq.kvq_quantize_append(c, -k_last, -v_last, None, start, w.B, 1))
+    torch.cuda.synchronize()
+    out = torch.full_like(ref, math.nan)
+    p = cfg.params(S.seq_lens_t)
+    p.fresh_tokens = 1
+    kvq.check(kvq.kvq_quantize_append(c, k_last, v_last, None, start, w.B, 1))
+    assert kvq.kvq_decode_noalloc(c, p, S.q_t, out) == kvq.KVQ_OK
+    torch.cuda.synchronize()
+    assert_f32_close(out.cpu().numpy(), ref.cpu().numpy().astype(np.float64), "fresh_tokens=1")
