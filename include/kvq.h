@@ -104,11 +104,25 @@ typedef struct kvq_cache {
   void* v_bscale;            /* (device) NVFP4 only, 16-byte aligned */
   float k_scale;             /* FP8 scale or NVFP4 global scale, finite > 0 */
   float v_scale;             /* as k_scale (ignored for MLA) */
+                             /* (both ignored where per-head scales are given) */
   const int32_t* block_table;/* (device) [batch][max_pages_per_seq] */
   int32_t max_pages_per_seq; /* >= 1 */
   int32_t rope_dim;          /* MLA: 64; otherwise 0 */
   void* k_pe;                /* (device) MLA only: bf16 rope keys */
   int32_t v_is_k_latent;     /* MLA: 1; otherwise 0 */
+  /*
+   * Per-kv-head scales (compressed-tensors PR 436, "attn_head" strategy: one
+   * static scale per attention head).  Optional, (device) float
+   * [num_kv_heads] each: when non-NULL, kv head h of K (V) uses
+   * k_head_scale[h] (v_head_scale[h]) wherever k_scale (v_scale) appears
+   * above -- the FP8 scale or the NVFP4 global scale -- in the append and in
+   * the decode, and k_scale (v_scale) is ignored.  Every entry must be
+   * finite and > 0 (not checked: device memory).  They are read like the
+   * block table, so nothing still running may write them (fresh_tokens).
+   * Not for MLA (one latent kv head: use k_scale).
+   */
+  const float* k_head_scale;
+  const float* v_head_scale;
 } kvq_cache;
 
 /* Parameters of one decode step (shared by partial and combine). */

@@ -79,16 +79,18 @@ kvq_status check_cache(const kvq_cache* c) {
   if ((long long)c->num_pages * c->num_kv_heads * c->page_size >= (1LL << 31))
     return KVQ_ERR_UNSUPPORTED;
   if (!c->block_table || !c->k_codes || !aligned16(c->k_codes)) return KVQ_ERR_INVALID;
-  if (!finite_pos(c->k_scale)) return KVQ_ERR_INVALID;
+  if (!c->k_head_scale && !finite_pos(c->k_scale)) return KVQ_ERR_INVALID;
   if (c->fmt == KVQ_NVFP4 && (!c->k_bscale || !aligned16(c->k_bscale))) return KVQ_ERR_INVALID;
   if (is_mla(c)) {
     if (c->rope_dim % 8 != 0 || !c->k_pe || !aligned16(c->k_pe)) return KVQ_ERR_INVALID;
     if (c->v_codes || !c->v_is_k_latent) return KVQ_ERR_INVALID;
+    if (c->k_head_scale || c->v_head_scale) return KVQ_ERR_INVALID;
     if (c->num_kv_heads != 1) return KVQ_ERR_INVALID;
     if (c->fmt != KVQ_NVFP4) return KVQ_ERR_UNSUPPORTED;
   } else {
     if (c->rope_dim != 0 || c->k_pe || c->v_is_k_latent) return KVQ_ERR_INVALID;
-    if (!c->v_codes || !aligned16(c->v_codes) || !finite_pos(c->v_scale)) return KVQ_ERR_INVALID;
+    if (!c->v_codes || !aligned16(c->v_codes)) return KVQ_ERR_INVALID;
+    if (!c->v_head_scale && !finite_pos(c->v_scale)) return KVQ_ERR_INVALID;
     if (c->fmt == KVQ_NVFP4 && (!c->v_bscale || !aligned16(c->v_bscale))) return KVQ_ERR_INVALID;
   }
   return KVQ_OK;
@@ -262,6 +264,8 @@ kvq_status kvq_quantize_append(const kvq_cache* c, const void* k_new, const void
   // fp32 reciprocal (53 >= 2 * 24 + 2)
   a.k_recip = (float)(1.0 / (double)c->k_scale);
   a.v_recip = is_mla(c) ? a.k_recip : (float)(1.0 / (double)c->v_scale);
+  a.k_hs = c->k_head_scale;
+  a.v_hs = c->v_head_scale;
   a.has_v = is_mla(c) ? 0 : 1;
   return cuda_status(launch_append(a, as_stream(stream)));
 }
@@ -357,6 +361,9 @@ kvq_status decode_impl(const kvq_cache* c, const kvq_decode_params* p, const voi
   a.Dv = p->v_dim;
   a.score_floats = (int)score_floats;
   a.qk_scale_log2 = p->sm_scale * c->k_scale * 1.4426950408889634f;
+  a.sm_scale = p->sm_scale;
+  a.k_hs = c->k_head_scale;
+  a.v_hs = c->v_head_scale;
   a.prob_scale = p->prob_scale;
   if (probq) a.prob_fast = prob_reciprocal_ok(p->prob_scale, &a.prob_recip) ? 1 : 0;
   a.fresh = p->fresh_tokens;

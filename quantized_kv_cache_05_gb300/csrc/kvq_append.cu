@@ -52,6 +52,20 @@ __device__ __forceinline__ long cache_row(const AppendArgs& a, int b, int pos, i
 // infinities and the canonical NaN -- the IEEE division gives all N.  Either
 // way every code equals the code of the correctly rounded quotient.
 template <int N>
+struct Floats {
+  float v[N];
+};
+
+// The IEEE quotients of a whole group: out of line, so that the rarely taken
+// fallback stays off the common path (not merged into it as predicated code).
+template <int N>
+__device__ __noinline__ Floats<N> ieee_quotients(Floats<N> x, float s) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) x.v[i] = __fdiv_rn(x.v[i], s);
+  return x;
+}
+
+template <int N>
 __device__ __forceinline__ void quotients_for_codes(float (&x)[N], float s, float z,
                                                     uint32_t lowmask) {
   float q[N];
@@ -64,8 +78,12 @@ __device__ __forceinline__ void quotients_for_codes(float (&x)[N], float s, floa
     m = min(m, (__float_as_uint(q[i]) + 1u) & lowmask);
   }
   if (m <= 2u) {
+    Floats<N> in;
 #pragma unroll
-    for (int i = 0; i < N; ++i) x[i] = __fdiv_rn(x[i], s);
+    for (int i = 0; i < N; ++i) in.v[i] = x[i];
+    const Floats<N> out = ieee_quotients<N>(in, s);
+#pragma unroll
+    for (int i = 0; i < N; ++i) x[i] = out.v[i];
   } else {
 #pragma unroll
     for (int i = 0; i < N; ++i) x[i] = q[i];
@@ -105,10 +123,13 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(const AppendArgs a) {
   const long dst_row = cache_row(a, ix.b, __ldg(a.start_pos + ix.b) + ix.tt, ix.h);
   if (dst_row < 0) return;
   uint8_t* dst = ix.isv ? a.v_codes : a.k_codes;
+  // the tensor's scale, or kv head h's (then its reciprocal here)
+  const float* hs = ix.isv ? a.v_hs : a.k_hs;
+  const float s = hs ? __ldg(hs + ix.h) : (ix.isv ? a.v_scale : a.k_scale);
+  const float z = hs ? __frcp_rn(s) : (ix.isv ? a.v_recip : a.k_recip);
   float f[8];
   bf16x8_to_f32(x, f);
-  quotients_for_codes<8>(f, ix.isv ? a.v_scale : a.k_scale, ix.isv ? a.v_recip : a.k_recip,
-                         kE4m3Low);
+  quotients_for_codes<8>(f, s, z, kE4m3Low);
   const uint32_t lo = f32x2_to_e4m3x2(f[0], f[1]) | (f32x2_to_e4m3x2(f[2], f[3]) << 16);
   const uint32_t hi = f32x2_to_e4m3x2(f[4], f[5]) | (f32x2_to_e4m3x2(f[6], f[7]) << 16);
   *reinterpret_cast<uint2*>(dst + dst_row * a.D + ix.part * 8) = make_uint2(lo, hi);
@@ -150,7 +171,8 @@ __global__ void __launch_bounds__(256) append_nvfp4_kernel(const AppendArgs a) {
   bf16x8_to_f32(x1, f + 8);
   uint32_t w0, w1;
   uint8_t sc;
-  nvfp4_block(f, ix.isv ? a.v_scale : a.k_scale, w0, w1, sc);
+  const float* hs = ix.isv ? a.v_hs : a.k_hs;   // kv head h's global scale, if given
+  nvfp4_block(f, hs ? __ldg(hs + ix.h) : (ix.isv ? a.v_scale : a.k_scale), w0, w1, sc);
   uint8_t* codes = ix.isv ? a.v_codes : a.k_codes;
   uint8_t* scales = ix.isv ? a.v_bscale : a.k_bscale;
   *reinterpret_cast<uint2*>(codes + dst_row * (a.D / 2) + ix.part * 8) = make_uint2(w0, w1);

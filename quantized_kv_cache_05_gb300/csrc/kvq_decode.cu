@@ -209,6 +209,13 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
   }
 
   const int hq0 = h * a.G;
+  // score and output factors of this kv head: the tensor's scales, or the
+  // head's own (per-kv-head scales)
+  const float qk_scale_log2 =
+      a.k_hs ? (a.sm_scale * __ldg(a.k_hs + h)) * 1.4426950408889634f : a.qk_scale_log2;
+  const float out_mult =
+      a.v_hs ? (a.prob_scale > 0.f ? __ldg(a.v_hs + h) * a.prob_scale : __ldg(a.v_hs + h))
+             : a.out_mult;
   // Q^T fragments (B operand of S^T = K Q^T: k = head dims, n = query heads
   // g + 8 hh), head dims permuted like the K fragments.  Each head is scaled
   // by its power of two 2^e (q_prescale_exp) before the f16 conversion, so
@@ -241,7 +248,7 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
       qb[j][hh][0] = pack_f16x2(__uint_as_float(v.x << 16) * f, __uint_as_float(v.x & 0xFFFF0000u) * f);
       qb[j][hh][1] = pack_f16x2(__uint_as_float(v.y << 16) * f, __uint_as_float(v.y & 0xFFFF0000u) * f);
     }
-    const float my = scale_pow2(a.qk_scale_log2, -e);   // head g + 8hh
+    const float my = scale_pow2(qk_scale_log2, -e);   // head g + 8hh
     qsc[hh][0] = __shfl_sync(0xffffffffu, my, 4 * (2 * t));
     qsc[hh][1] = __shfl_sync(0xffffffffu, my, 4 * (2 * t + 1));
   }
@@ -513,7 +520,7 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
     for (int w = 0; w < kDecodeWarps; ++w)
       sm.fac[w][row] = (M == -INFINITY || sm.m[w][row] == -INFINITY || Ltot == 0.f)
                            ? 0.f
-                           : ex2(sm.m[w][row] - M) / Ltot * a.out_mult;
+                           : ex2(sm.m[w][row] - M) / Ltot * out_mult;
     float lse = (M == -INFINITY || Ltot == 0.f) ? -INFINITY : (M + log2f(Ltot)) * kLn2;
     if (bad) lse = NAN;
     a.part_lse[(part_row + row) * a.num_splits + split] = lse;

@@ -37,6 +37,8 @@ struct AppendArgs {
   uint16_t* k_pe;
   float k_scale, v_scale;
   float k_recip, v_recip;     // RN(1 / scale) of the FP8 scales
+  const float* k_hs;          // per-kv-head scales (replace k_scale, v_scale) or null
+  const float* v_hs;
   int has_v;
 };
 
@@ -54,6 +56,9 @@ struct PartialArgs {
   int Dv;                     // value dim (the partials' row length)
   int score_floats;           // FP8-prob mode: scores one chunk needs (<= kScoreCapacity)
   float qk_scale_log2;        // sm_scale * k_scale * log2(e)
+  float sm_scale;             // with per-kv-head scales: the kernel forms the above per head
+  const float* k_hs;          // per-kv-head scales (replace k_scale, v_scale) or null
+  const float* v_hs;
   float pe_scale_log2;        // MLA rope part: sm_scale * log2(e)
   float out_mult;             // v_scale (times prob_scale with FP8 probabilities)
   float prob_scale;           // > 0: FP8 probabilities

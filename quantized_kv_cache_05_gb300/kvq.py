@@ -38,6 +38,7 @@ class kvq_cache(ctypes.Structure):
         ("head_dim", _i32), ("k_codes", _P), ("v_codes", _P), ("k_bscale", _P),
         ("v_bscale", _P), ("k_scale", _f), ("v_scale", _f), ("block_table", _P),
         ("max_pages_per_seq", _i32), ("rope_dim", _i32), ("k_pe", _P), ("v_is_k_latent", _i32),
+        ("k_head_scale", _P), ("v_head_scale", _P),
     ]
 
 

@@ -28,7 +28,9 @@ class QuantizedKVCache:
 
     def __init__(self, fmt: str, num_pages: int, page_size: int, num_kv_heads: int,
                  head_dim: int, block_table: torch.Tensor, k_scale: float, v_scale: float,
-                 rope_dim: int = 0, device: str | torch.device = "cuda"):
+                 rope_dim: int = 0, device: str | torch.device = "cuda",
+                 k_head_scale: Optional[torch.Tensor] = None,
+                 v_head_scale: Optional[torch.Tensor] = None):
         self.fmt = fmt
         self.num_pages, self.page_size = num_pages, page_size
         self.Hkv, self.D, self.rope = num_kv_heads, head_dim, rope_dim
@@ -47,6 +49,14 @@ class QuantizedKVCache:
                                  device=device) if rope_dim else None)
         self.block_table = block_table.to(device=device, dtype=torch.int32).contiguous()
         self.max_pages_per_seq = self.block_table.shape[1]
+        # per-kv-head scales (float32 [Hkv] on the device), replacing k_scale / v_scale
+        def _hs(t):
+            if t is None:
+                return None
+            t = t.to(device=device, dtype=torch.float32).contiguous()
+            assert t.numel() == num_kv_heads, "one scale per kv head"
+            return t
+        self.k_head_scale, self.v_head_scale = _hs(k_head_scale), _hs(v_head_scale)
 
     @property
     def mla(self) -> bool:
@@ -67,6 +77,8 @@ class QuantizedKVCache:
         c.rope_dim = self.rope
         c.k_pe = self.k_pe.data_ptr() if self.k_pe is not None else None
         c.v_is_k_latent = 1 if self.mla else 0
+        c.k_head_scale = self.k_head_scale.data_ptr() if self.k_head_scale is not None else None
+        c.v_head_scale = self.v_head_scale.data_ptr() if self.v_head_scale is not None else None
         return c
 
     def append(self, k_new: torch.Tensor, v_new: Optional[torch.Tensor],

@@ -163,6 +163,8 @@ class Workload:
     out: str = "f32"         # "f32", "bf16" or "e4m3"
     splits: tuple = (1,)
     permute_pages: bool = False
+    head_scales: bool = False     # per-kv-head static scales ("attn_head" strategy)
+    head_exp: tuple = ()          # K/V of kv head h times 2^head_exp[h % len] (exact)
 
     @property
     def mla(self) -> bool:
@@ -222,8 +224,17 @@ class Workload:
             t1 = int(self.seq_lens[b])
         row = self.Hkv * self.D
         off = (b * self.Lmax + t0) * row
-        return self._fill(tensor, (t1 - t0) * row, off, self.D).reshape(t1 - t0, self.Hkv,
-                                                                          self.D)
+        r = self._fill(tensor, (t1 - t0) * row, off, self.D).reshape(t1 - t0, self.Hkv, self.D)
+        return self._head_skew(r)
+
+    def _head_skew(self, r: np.ndarray) -> np.ndarray:
+        """Multiply kv head h of rows [T][Hkv][D] (bf16 bits) by 2^head_exp[h]:
+        an exponent shift, exact while the result stays a normal bf16."""
+        if not self.head_exp:
+            return r
+        e = np.array([self.head_exp[h % len(self.head_exp)] for h in range(self.Hkv)], np.int32)
+        x = bf16_to_f32(r) * np.exp2(e.astype(np.float32))[None, :, None]
+        return f32_to_bf16(x)
 
     def kpe_rows(self, b: int, t0: int = 0, t1: Optional[int] = None) -> np.ndarray:
         if t1 is None:
@@ -238,7 +249,8 @@ class Workload:
             n = self.B * self.Lmax * self.rope
             return fill_bf16(self.seed, T_KPE, n).reshape(self.B, self.Lmax, self.rope)
         n = self.B * self.Lmax * self.Hkv * self.D
-        return self._fill(tensor, n, 0, self.D).reshape(self.B, self.Lmax, self.Hkv, self.D)
+        r = self._fill(tensor, n, 0, self.D).reshape(self.B * self.Lmax, self.Hkv, self.D)
+        return self._head_skew(r).reshape(self.B, self.Lmax, self.Hkv, self.D)
 
     def pages_per_seq(self) -> int:
         ps = self.page_size or max(16, -(-self.Lmax // 16) * 16)
@@ -292,6 +304,16 @@ def paged_fp8_probs(B: int = 64, lo: int = 512, hi: int = 8192, seed: int = 0) -
     lens = uniform_lengths(seed, B, lo, hi)
     return Workload("paged_fp8_probs", "fp8", B, 16, 16, 128, lens, page_size=16,
                     permute_pages=True, prob_fp8=True, out="e4m3", splits=(1, 0), seed=seed)
+
+
+def gqa_fp8_head_scales(L: int = 8192) -> Workload:
+    """The GQA FP8 workload with per-kv-head static scales (compressed-tensors
+    PR 436 "attn_head" strategy): same shapes and values, one scale per kv
+    head from that head's amax."""
+    w = gqa_fp8(L)
+    w.name = f"gqa_fp8_head_L{L}"
+    w.head_scales = True
+    return w
 
 
 def mla_nvfp4(B: int = 32, L: int = 4096) -> Workload:

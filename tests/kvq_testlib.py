@@ -58,10 +58,24 @@ class Setup:
         kvq.check(st1)
         kvq.check(st2)
         self.gpu_k_scale, self.gpu_v_scale = gk, gv
+        # per-kv-head scales ("attn_head"): oracle over all requests' rows of a
+        # head; product: the amax kernel on each head's rows, then the scale call
+        self.k_head = self.v_head = None
+        khs = vhs = None
+        if getattr(w, "head_scales", False):
+            hsc = oracle.fp8_head_scales if w.fmt == "fp8" else oracle.nvfp4_head_scales
+            kall = np.concatenate(self.k, axis=0)
+            vall = np.concatenate(self.v, axis=0)
+            self.k_head, self.v_head = hsc(kall), hsc(vall)
+            khs = self._gpu_head_scales(kall, fmt)
+            vhs = self._gpu_head_scales(vall, fmt)
+            assert np.array_equal(khs, self.k_head) and np.array_equal(vhs, self.v_head)
+            khs, vhs = torch.from_numpy(khs), torch.from_numpy(vhs)
 
         # --- device cache, filled request by request through the append call
         self.cache = runtime.QuantizedKVCache(w.fmt, npages, self.ps, Hkv, D, torch.from_numpy(bt),
-                                              gk, gv, rope_dim=w.rope, device=device)
+                                              gk, gv, rope_dim=w.rope, device=device,
+                                              k_head_scale=khs, v_head_scale=vhs)
         zero = torch.zeros(1, dtype=torch.int32, device=device)
         for b in range(B):
             if int(w.seq_lens[b]) == 0:
@@ -77,6 +91,15 @@ class Setup:
         self.seq_lens_t = torch.from_numpy(np.ascontiguousarray(w.seq_lens, np.int32)).to(device)
         torch.cuda.synchronize()
         self._host_cache = None
+
+    def _gpu_head_scales(self, rows: np.ndarray, fmt: int) -> np.ndarray:
+        out = []
+        for h in range(rows.shape[1]):
+            a = self._gpu_amax([np.ascontiguousarray(rows[:, h])])
+            st, s = kvq.kvq_tensor_scale(fmt, a)
+            kvq.check(st)
+            out.append(s)
+        return np.array(out, np.float32)
 
     def _gpu_amax(self, rows) -> float:
         flat = np.concatenate([r.reshape(-1) for r in rows]) if rows else np.zeros(0, np.uint16)
@@ -109,8 +132,21 @@ class Setup:
         return hc[pages, kvh, pos % self.ps]
 
     # --------------------------------------------------------- oracle view
+    def oracle_scale(self, which: str, kvh: int) -> float:
+        heads = self.k_head if which == "k" else self.v_head
+        if heads is not None:
+            return float(heads[kvh])
+        return self.k_scale if which == "k" else self.v_scale
+
     def oracle_codes(self, which: str, b: int, kvh: int = 0):
-        x = (self.k if which == "k" else self.v)[b][:, kvh, :]
+        rows = (self.k if which == "k" else self.v)[b]
+        heads = self.k_head if which == "k" else self.v_head
+        if heads is not None:   # per-kv-head quantizers on all heads, this head's slice
+            if self.w.fmt == "fp8":
+                return oracle.fp8_quantize_heads(rows, heads)[:, kvh], None
+            c, bs = oracle.nvfp4_quantize_heads(rows, heads)
+            return c[:, kvh], bs[:, kvh]
+        x = rows[:, kvh, :]
         s = self.k_scale if which == "k" else self.v_scale
         if self.w.fmt == "fp8":
             return oracle.fp8_quantize(x, s), None
@@ -118,7 +154,7 @@ class Setup:
 
     def oracle_dequant(self, which: str, b: int, kvh: int = 0) -> np.ndarray:
         codes, bs = self.oracle_codes(which, b, kvh)
-        s = self.k_scale if which == "k" else self.v_scale
+        s = self.oracle_scale(which, kvh)
         if self.w.fmt == "fp8":
             return oracle.fp8_dequant(codes, s)
         return oracle.nvfp4_dequant(codes, bs, s)

@@ -251,3 +251,20 @@ def test_nvfp4_head_dims_refused_before_launch(L, D, want):
     p.qk_dim = p.v_dim = D
     assert kvq.kvq_decode_partial(c, p, 0x50000, 0x60000, 0x70000, None) == want
     assert kvq.kvq_decode(c, p, 0x50000, 0x60000, 0x70000, 0x90000, 0x80000, None) == want
+
+
+def test_head_scale_fields(L):
+    """Per-kv-head scales replace the per-tensor ones (which may then be
+    anything) and are refused for the MLA latent cache."""
+    c, p = good_cache(), good_params()
+    c.k_head_scale, c.v_head_scale = 0xC0000, 0xD0000
+    c.k_scale = c.v_scale = 0.0
+    c.head_dim, c.num_kv_heads = 96, 2   # an unsupported dim: refused after the scale checks
+    p.qk_dim = p.v_dim = 96
+    assert kvq.kvq_decode_partial(c, p, 0x50000, 0x60000, 0x70000, None) == kvq.KVQ_ERR_UNSUPPORTED
+    c.k_head_scale = None                # back to the per-tensor k_scale = 0: invalid
+    assert kvq.kvq_decode_partial(c, p, 0x50000, 0x60000, 0x70000, None) == kvq.KVQ_ERR_INVALID
+    m = nvfp4_cache(512)
+    m.num_kv_heads, m.v_codes, m.v_bscale, m.rope_dim, m.k_pe, m.v_is_k_latent = 1, None, None, 64, 0xE0000, 1
+    m.k_head_scale = 0xC0000
+    assert kvq.kvq_quantize_append(m, 0x1000, None, 0x4000, 0x3000, 1, 1, None) == kvq.KVQ_ERR_INVALID
