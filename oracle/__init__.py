@@ -262,6 +262,29 @@ def nvfp4_quantize_heads(x_bf16: np.ndarray, gs) -> tuple[np.ndarray, np.ndarray
     return codes, sc
 
 
+# --------------------------------------------------------------------------
+# FP8 query (compressed-tensors PR 436: "QKV-FP8-Tensor" / "QKV-FP8-Head",
+# a query observer next to the K and V ones; vLLM PR 15734: QK quantization
+# in the attention loop).  The query is quantized like K: E4M3(fl32(q / s))
+# with a static scale per tensor or per query head, and the scores use the
+# dequantized query.
+# --------------------------------------------------------------------------
+
+def fp8_query(q_bf16: np.ndarray, scales) -> tuple[np.ndarray, np.ndarray]:
+    """q [B][Hq][D] bf16 and one scale (per tensor) or Hq scales (per query
+    head) -> (E4M3 codes [B][Hq][D], dequantized q in float64)."""
+    q = _c(q_bf16, np.uint16)
+    sc = np.atleast_1d(np.asarray(scales, np.float32))
+    if sc.size == 1:
+        codes = fp8_quantize(q, float(sc[0]))
+        return codes, fp8_dequant(codes, float(sc[0]))
+    codes = fp8_quantize_heads(q, sc)
+    deq = np.empty(q.shape, np.float64)
+    for h in range(q.shape[1]):
+        deq[:, h] = fp8_dequant(np.ascontiguousarray(codes[:, h]), float(sc[h]))
+    return codes, deq
+
+
 def fp8_dequant(codes: np.ndarray, scale: float) -> np.ndarray:
     c = _c(codes, np.uint8)
     out = np.empty(c.shape, np.float64)
