@@ -348,6 +348,26 @@ def attention_partial_probq(q, k, v, start: int, end: int, sm_scale: float,
     return out, lse.value
 
 
+def prefill_attention(q, k, v, sm_scale: float) -> tuple[np.ndarray, np.ndarray]:
+    """Causal attention of Tq new query tokens over a cache of L tokens that
+    already holds them (Model-Optimizer PR 1832: the prefill kernel that its
+    latency tables compare with split decode).  Query i sits at position
+    L - Tq + i and attends to keys [0, L - Tq + i]: exact attention per query
+    over that prefix.  q [Tq][Dqk], k [L][Dqk], v [L][Dv] (float64) ->
+    (out [Tq][Dv], lse [Tq])."""
+    q = _c(q, np.float64)
+    k = _c(k, np.float64)
+    v = _c(v, np.float64)
+    Tq, L = q.shape[0], k.shape[0]
+    assert Tq <= L, "the cache holds the new tokens"
+    out = np.empty((Tq, v.shape[1]), np.float64)
+    lse = np.empty(Tq, np.float64)
+    for i in range(Tq):
+        n = L - Tq + i + 1
+        out[i], lse[i] = attention_exact(q[i], k[:n], v[:n], sm_scale)
+    return out, lse
+
+
 def combine(o_parts, lse) -> np.ndarray:
     o = _c(o_parts, np.float64)
     l = _c(lse, np.float64)
