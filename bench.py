@@ -66,7 +66,8 @@ def hbm_peak():
 
 
 KERNEL_SOURCES = {
-    "decode": ["kvq_decode.cu", "kvq_attn.cuh", "kvq_device.cuh", "kvq_internal.h"],
+    "decode": ["kvq_decode.cuh", "kvq_decode.cu", "kvq_decode_nvfp4.cu", "kvq_attn.cuh",
+               "kvq_device.cuh", "kvq_internal.h"],
     "mla": ["kvq_mla.cu", "kvq_attn.cuh", "kvq_device.cuh", "kvq_internal.h"],
 }
 
@@ -203,8 +204,24 @@ class Bench:
                 dev_rows[t] = rows
             ks = kvq.kvq_tensor_scale(fmt, amax[synth.T_K])[1]
             vs = kvq.kvq_tensor_scale(fmt, amax.get(synth.T_V, amax[synth.T_K]))[1]
+            head_sc = {}
+            if getattr(w, "head_scales", False):
+                # per-kv-head scales: the amax kernel on each head's rows
+                for t in tensors:
+                    hs = []
+                    for h in range(Hkv):
+                        m = 0.0
+                        for x in dev_rows[t]:
+                            xh = x[:, h].contiguous()
+                            a = torch.zeros(1, dtype=torch.float32, device=device)
+                            kvq.check(kvq.kvq_amax_bf16(xh, xh.numel(), a, self.stream))
+                            m = max(m, float(a.item()))
+                        hs.append(kvq.kvq_tensor_scale(fmt, m)[1])
+                    head_sc[t] = torch.tensor(hs, dtype=torch.float32)
             self.cache = runtime.QuantizedKVCache(w.fmt, npages, ps, Hkv, D, torch.from_numpy(bt),
-                                                  ks, vs, rope_dim=w.rope, device=device)
+                                                  ks, vs, rope_dim=w.rope, device=device,
+                                                  k_head_scale=head_sc.get(synth.T_K),
+                                                  v_head_scale=head_sc.get(synth.T_V))
             zero = torch.zeros(1, dtype=torch.int32, device=device)
             kpe_rows = [self._bf16(w.kpe_rows(b)) for b in range(B)] if w.mla else None
             for b in range(B):
@@ -230,6 +247,19 @@ class Bench:
             # buffer, so that the end-to-end step moves them with one copy
             self._pack_inputs()
         self.stream.synchronize()
+        self.q_scale = 1.0
+        self.q_codes = None
+        if getattr(w, "q_fp8", False):
+            # FP8 query: per-tensor scale from the amax kernel, codes from
+            # kvq_quantize_fp8 (the step then reads the codes)
+            with torch.cuda.stream(self.stream):
+                a = torch.zeros(1, dtype=torch.float32, device=device)
+                kvq.check(kvq.kvq_amax_bf16(self.q, self.q.numel(), a, self.stream))
+                self.q_scale = kvq.kvq_tensor_scale(kvq.KVQ_FP8_E4M3, float(a.item()))[1]
+                self.q_codes = torch.empty(self.q.shape, dtype=torch.uint8, device=device)
+                kvq.check(kvq.kvq_quantize_fp8(self.q, self.q.numel(), self.q_scale, None, 0, 0,
+                                               self.q_codes, self.stream))
+            self.stream.synchronize()
         self.splits = splits or runtime.auto_splits(B, Hkv, w.G, w.Lmax, w.fmt, device)
         self.out_scale = 1.0
         if w.out == "e4m3":
@@ -274,8 +304,11 @@ class Bench:
 
     def _cfg(self, out, out_scale):
         w = self.w
-        return self.runtime.DecodeConfig(w.B, w.Hq, w.Dqk, w.Dv, getattr(self, "splits", 1),
-                                         w.Lmax, w.sm_scale, w.prob_scale, out, out_scale)
+        cfg = self.runtime.DecodeConfig(w.B, w.Hq, w.Dqk, w.Dv, getattr(self, "splits", 1),
+                                        w.Lmax, w.sm_scale, w.prob_scale, out, out_scale)
+        if getattr(self, "q_codes", None) is not None:
+            cfg.q_fp8, cfg.q_scale = True, self.q_scale
+        return cfg
 
     def _launch(self, full: bool, stream, io=None):
         """full: append + kvq_decode (one step); else kvq_decode alone.  io:
@@ -285,11 +318,48 @@ class Bench:
         c = self.cache.struct()
         p = self.cfg.params(self.seq_lens)
         q, k, v, kpe, out = io or (self.q, self.k_new, self.v_new, self.kpe_new, self.ws.out)
+        if self.q_codes is not None and io is None:
+            q = self.q_codes
         if full:
             kvq.check(kvq.kvq_quantize_append(c, k, v, kpe, self.start_pos, self.w.B, 1, stream))
             p.fresh_tokens = 1   # the decode overlaps with the append of the last position
         kvq.check(kvq.kvq_decode(c, p, q, self.ws.part_o, self.ws.part_lse, self.ws.counters,
                                  out, stream))
+
+    def _launch_prefill(self, full: bool, stream):
+        """The same step with the non-split prefill kernel (kvq_prefill, one
+        query token per request) in place of the split decode."""
+        kvq = self.kvq
+        c = self.cache.struct()
+        p = self.cfg.params(self.seq_lens)
+        if full:
+            kvq.check(kvq.kvq_quantize_append(c, self.k_new, self.v_new, self.kpe_new,
+                                              self.start_pos, self.w.B, 1, stream))
+        kvq.check(kvq.kvq_prefill(c, p, 1, self.q, self.ws.out, stream))
+
+    def time_prefill(self, steps: int, warmup: int):
+        """(step us: append + prefill as one graph, kernel us: one direct call)."""
+        t = self.torch
+        with t.cuda.stream(self.stream):
+            self._launch_prefill(True, self.stream)
+        self.stream.synchronize()
+        g = t.cuda.CUDAGraph()
+        with t.cuda.graph(g, stream=self.stream):
+            self._launch_prefill(True, t.cuda.current_stream())
+        step = statistics.mean(self.time_graph(g, steps, warmup))
+        times = []
+        with t.cuda.stream(self.stream):
+            for i in range(warmup + steps):
+                self.flush_l2(i)
+                e0 = t.cuda.Event(enable_timing=True)
+                e1 = t.cuda.Event(enable_timing=True)
+                e0.record(self.stream)
+                self._launch_prefill(False, self.stream)
+                e1.record(self.stream)
+                if i >= warmup:
+                    times.append((e0, e1))
+        self.stream.synchronize()
+        return step, statistics.mean([a.elapsed_time(b) * 1e3 for a, b in times])
 
     def _capture(self, full: bool):
         t = self.torch
@@ -582,7 +652,9 @@ def sweep(device, args):
     plans = [("gqa_fp8", synth.gqa_fp8, [1024, 8192, 32768], [1, 2, 4, 8, 0]),
              ("nvfp4", synth.nvfp4, [2048, 8192, 32768], [1, 2, 4, 8, 0]),
              ("paged_fp8_probs", lambda L: synth.paged_fp8_probs(), [0], [1, 2, 0]),
-             ("mla_nvfp4", lambda L: synth.mla_nvfp4(), [0], [1, 2, 4, 8, 0])]
+             ("mla_nvfp4", lambda L: synth.mla_nvfp4(), [0], [1, 2, 4, 8, 0]),
+             ("gqa_fp8_head_scales", synth.gqa_fp8_head_scales, [8192, 32768], [0]),
+             ("gqa_fp8_query", synth.gqa_fp8_query, [8192, 32768], [0])]
     for name, mk, lens, splits in plans:
         for L in lens:
             w = mk(L) if L else mk(None)
@@ -605,6 +677,18 @@ def sweep(device, args):
                             "kv_hbm_frac": round(kvb / (us * 1e-6) / 1e9 / peak, 3),
                             "kernel_us": round(ku, 2),
                             "kernel_hbm_frac": round(ab / (ku * 1e-6) / 1e9 / peak, 3)})
+            if base is not None and name in ("gqa_fp8", "nvfp4"):
+                # the pages' comparison: the non-split prefill kernel on the
+                # same decode step (one query token per request)
+                us, ku = base.time_prefill(args.sweep_steps, 3)
+                kvb = base.kv_bytes()
+                res.append({"workload": name, "kv_len": L, "s": "prefill",
+                            "us_per_step": round(us, 2),
+                            "kv_gbs": round(kvb / (us * 1e-6) / 1e9, 1),
+                            "kv_hbm_frac": round(kvb / (us * 1e-6) / 1e9 / peak, 3),
+                            "kernel_us": round(ku, 2),
+                            "kernel_hbm_frac": round(base.algorithmic_bytes() / (ku * 1e-6) / 1e9
+                                                     / peak, 3)})
             del base
     return res
 

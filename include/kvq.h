@@ -155,6 +155,20 @@ typedef struct kvq_decode_params {
    * method: a scheduling contract between two calls of this library.
    */
   int32_t fresh_tokens;
+  /*
+   * FP8 query (compressed-tensors PR 436: a query observer next to the K
+   * and V ones, GSM8K rows "QKV-FP8-Tensor" / "QKV-FP8-Head"; vLLM PR 15734:
+   * QK quantization in the attention loop).  q_fp8 = 0: q is bf16 (default).
+   * q_fp8 = 1: q holds E4M3 codes [batch][Hq][qk_dim] (kvq_quantize_fp8
+   * makes them) whose values are dec(code) * q_scale, or * q_head_scale[hq]
+   * when that (device, [num_q_heads]) array is given.  With an FP8 cache the
+   * scores run on E4M3 x E4M3 tensor-core MMAs straight from the cached
+   * codes; with an NVFP4 cache the codes are widened exactly to f16.  Not
+   * for MLA.
+   */
+  int32_t q_fp8;
+  float q_scale;             /* q_fp8 without q_head_scale: finite > 0 */
+  const float* q_head_scale; /* (device, optional) [num_q_heads] */
 } kvq_decode_params;
 
 /* Human-readable name of a status code (static string). */
@@ -268,6 +282,27 @@ kvq_status kvq_decode(const kvq_cache* c, const kvq_decode_params* p, const void
                       void* stream);
 
 /*
+ * Prefill attention over the cache (Model-Optimizer PR 1832: the prefill
+ * kernel of its latency tables, timed against split-KV decode): causal, no
+ * KV split.  Request b holds seq_lens[b] = L tokens, the last q_len of them
+ * the new ones whose queries are given: query i (position L - q_len + i)
+ * attends to keys 0 .. L - q_len + i,
+ *   out[b][i][hq][:] = sum_j softmax_j(sm_scale q . k^_j) v^_j
+ * in p->out_dtype (as kvq_decode_combine writes it).  With q_len = 1 this
+ * is one program per (request, kv head) over the whole sequence.
+ *   q   (device) bf16 [batch][q_len][Hq][head_dim], 16-byte aligned.
+ *   out (device) [batch][q_len][Hq][head_dim].
+ * Uses batch, num_q_heads, qk_dim = v_dim = head_dim, seq_lens, max_kv_len,
+ * sm_scale, out_dtype, out_scale and error_flag of p (num_splits and
+ * fresh_tokens are ignored; prob_scale must be 0 and q_fp8 0).  FP8 or
+ * NVFP4 caches with head_dim 64 or 128, per-kv-head scales allowed; not MLA.
+ * Requests with L < q_len: queries before position 0 attend to nothing and
+ * give 0.  q_len >= 1.
+ */
+kvq_status kvq_prefill(const kvq_cache* c, const kvq_decode_params* p, int q_len, const void* q,
+                       void* out, void* stream);
+
+/*
  * Allocation-free decode step (the pages have no counterpart; this is a
  * convenience of this library).  For callers that cannot allocate device
  * memory -- their device memory is owned by a host framework's fixed pool,
@@ -294,6 +329,18 @@ kvq_status kvq_decode(const kvq_cache* c, const kvq_decode_params* p, const void
 #define KVQ_NOALLOC_SCRATCH_BYTES (4u << 20)
 kvq_status kvq_decode_noalloc(const kvq_cache* c, const kvq_decode_params* p, const void* q,
                               void* out, void* stream);
+
+/*
+ * FP8 quantization of bf16 values (e.g. the query of an FP8-query decode):
+ *   out[i] = E4M3(fl32(x[i] / s)), s = head_scale[(i / head_len) % num_heads]
+ * when head_scale (device, [num_heads]) is given, else scale (finite > 0);
+ * round to nearest even, saturating at +-448, the sign of zero kept -- the
+ * arithmetic of the FP8 append.  x (device, bf16, 16-byte aligned) and out
+ * (device) hold n elements; n and head_len multiples of 8 (head_len > 0
+ * when head_scale is given).
+ */
+kvq_status kvq_quantize_fp8(const void* x, size_t n, float scale, const float* head_scale,
+                            int head_len, int num_heads, uint8_t* out, void* stream);
 
 /*
  * Elementwise fp32 -> code conversions with the device encoders the append

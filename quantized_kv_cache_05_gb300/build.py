@@ -12,7 +12,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvq.so")
-SOURCES = ["kvq_api.cu", "kvq_append.cu", "kvq_decode.cu", "kvq_mla.cu"]
+SOURCES = ["kvq_api.cu", "kvq_append.cu", "kvq_decode.cu", "kvq_decode_nvfp4.cu", "kvq_mla.cu",
+           "kvq_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # host code: no FP contraction (the host-side checks emulate device fp32
 # operations one by one)

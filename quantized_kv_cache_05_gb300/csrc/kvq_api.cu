@@ -108,6 +108,8 @@ kvq_status check_params(const kvq_decode_params* p) {
   if (p->out_dtype < KVQ_OUT_F32 || p->out_dtype > KVQ_OUT_E4M3) return KVQ_ERR_INVALID;
   if (p->out_dtype == KVQ_OUT_E4M3 && !finite_pos(p->out_scale)) return KVQ_ERR_INVALID;
   if (p->fresh_tokens < 0) return KVQ_ERR_INVALID;
+  if (p->q_fp8 != 0 && p->q_fp8 != 1) return KVQ_ERR_INVALID;
+  if (p->q_fp8 && !p->q_head_scale && !finite_pos(p->q_scale)) return KVQ_ERR_INVALID;
   return KVQ_OK;
 }
 
@@ -208,6 +210,20 @@ kvq_status kvq_encode_e4m3(const float* x, uint8_t* out, size_t n, void* stream)
 kvq_status kvq_encode_e2m1(const float* x, uint8_t* out, size_t n, void* stream) {
   if (n > 0 && (!x || !out)) return KVQ_ERR_INVALID;
   return cuda_status(launch_encode(1, x, out, n, as_stream(stream)));
+}
+
+kvq_status kvq_quantize_fp8(const void* x, size_t n, float scale, const float* head_scale,
+                            int head_len, int num_heads, uint8_t* out, void* stream) {
+  if (n == 0) return KVQ_OK;
+  if (!x || !out || !aligned16(x) || n % 8 != 0) return KVQ_ERR_INVALID;
+  if (head_scale) {
+    if (head_len <= 0 || head_len % 8 != 0 || num_heads <= 0) return KVQ_ERR_INVALID;
+  } else if (!finite_pos(scale)) {
+    return KVQ_ERR_INVALID;
+  }
+  const float z = head_scale ? 0.f : (float)(1.0 / (double)scale);
+  return cuda_status(launch_quantize_fp8(static_cast<const uint16_t*>(x), n, scale, z, head_scale,
+                                         head_len, num_heads, out, as_stream(stream)));
 }
 
 kvq_status kvq_encode_prob_e4m3(const float* p, uint8_t* out, size_t n, float prob_scale,
@@ -340,7 +356,10 @@ kvq_status decode_impl(const kvq_cache* c, const kvq_decode_params* p, const voi
   const uint64_t rows = (uint64_t)c->num_pages * c->num_kv_heads * c->page_size;
 
   PartialArgs a{};
-  a.q = static_cast<const uint16_t*>(q);
+  a.q = q;
+  a.q_fp8 = p->q_fp8;
+  a.q_scale = p->q_scale;
+  a.q_hs = p->q_fp8 ? p->q_head_scale : nullptr;
   a.k_bscale = static_cast<const uint8_t*>(c->k_bscale);
   a.v_bscale = static_cast<const uint8_t*>(c->v_bscale);
   a.k_pe = static_cast<const uint16_t*>(c->k_pe);
@@ -375,7 +394,7 @@ kvq_status decode_impl(const kvq_cache* c, const kvq_decode_params* p, const voi
   if (is_mla(c)) {
     if (D != 512 || c->rope_dim != 64 || G != 16 || p->qk_dim != 576 || p->v_dim != 512)
       return KVQ_ERR_UNSUPPORTED;
-    if (probq) return KVQ_ERR_UNSUPPORTED;
+    if (probq || p->q_fp8) return KVQ_ERR_UNSUPPORTED;
     a.out_mult = c->k_scale;   // the values are the latent itself
     a.pe_scale_log2 = p->sm_scale * 1.4426950408889634f;
     // latent codes as two 128-byte halves per row, rope keys as 128-byte rows,
@@ -439,6 +458,59 @@ kvq_status kvq_decode_combine(const kvq_decode_params* p, const float* part_o,
   a.out_dtype = p->out_dtype;
   a.out_scale = p->out_scale;
   return cuda_status(launch_combine(a, as_stream(stream)));
+}
+
+kvq_status kvq_prefill(const kvq_cache* c, const kvq_decode_params* p, int q_len, const void* q,
+                       void* out, void* stream) {
+  kvq_status s = check_cache(c);
+  if (s != KVQ_OK) return s;
+  s = check_params(p);
+  if (s != KVQ_OK) return s;
+  if (q_len < 1) return KVQ_ERR_INVALID;
+  if (p->batch == 0) return KVQ_OK;
+  if (!q || !aligned16(q) || !out) return KVQ_ERR_INVALID;
+  if (p->num_q_heads % c->num_kv_heads != 0) return KVQ_ERR_INVALID;
+  if (is_mla(c) || p->prob_scale > 0.f || p->q_fp8) return KVQ_ERR_UNSUPPORTED;
+  const int D = c->head_dim;
+  if (p->qk_dim != D || p->v_dim != D) return KVQ_ERR_INVALID;
+  if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
+  if ((long long)p->max_kv_len > (long long)c->max_pages_per_seq * c->page_size)
+    return KVQ_ERR_INVALID;
+  const int G = p->num_q_heads / c->num_kv_heads;
+  if ((long long)q_len * G >= (1LL << 30) || (long long)p->batch * c->num_kv_heads > 65535)
+    return KVQ_ERR_UNSUPPORTED;
+  PartialArgs a{};
+  a.q = q;
+  a.k_bscale = static_cast<const uint8_t*>(c->k_bscale);
+  a.v_bscale = static_cast<const uint8_t*>(c->v_bscale);
+  a.block_table = c->block_table;
+  a.seq_lens = p->seq_lens;
+  a.error_flag = p->error_flag;
+  a.batch = p->batch;
+  a.Hq = p->num_q_heads;
+  a.Hkv = c->num_kv_heads;
+  a.G = G;
+  a.ps = c->page_size;
+  a.max_pages = c->max_pages_per_seq;
+  a.num_pages = c->num_pages;
+  a.max_kv_len = p->max_kv_len;
+  a.Dv = D;
+  a.q_len = q_len;
+  a.qk_scale_log2 = p->sm_scale * c->k_scale * 1.4426950408889634f;
+  a.sm_scale = p->sm_scale;
+  a.k_hs = c->k_head_scale;
+  a.v_hs = c->v_head_scale;
+  a.out_mult = c->v_scale;
+  a.out = out;
+  a.out_dtype = p->out_dtype;
+  a.out_scale = p->out_scale;
+  const uint64_t rows = (uint64_t)c->num_pages * c->num_kv_heads * c->page_size;
+  const uint64_t row_bytes = c->fmt == KVQ_FP8_E4M3 ? D : D / 2;
+  TensorMaps maps;
+  if (!make_row_map(&maps.k16, c->k_codes, row_bytes, rows) ||
+      !make_row_map(&maps.v16, c->v_codes, row_bytes, rows))
+    return KVQ_ERR_CUDA;
+  return cuda_status(launch_prefill(c->fmt, D, maps, a, as_stream(stream)));
 }
 
 }  // extern "C"

@@ -230,6 +230,29 @@ __global__ void __launch_bounds__(256) encode_kernel(int kind, const float* x, u
   }
 }
 
+// FP8 quantizer of a bf16 array, 8 elements per thread (the append's
+// arithmetic); s per tensor or per head of head_len elements.
+__global__ void __launch_bounds__(256) quantize_fp8_kernel(const uint16_t* x, size_t n8,
+                                                           float scale, float recip,
+                                                           const float* head_scale, int head_len,
+                                                           int num_heads, uint8_t* out) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const uint4 v = reinterpret_cast<const uint4*>(x)[i];
+    float s = scale, z = recip;
+    if (head_scale) {
+      s = __ldg(head_scale + (int)((i * 8 / (size_t)head_len) % (size_t)num_heads));
+      z = __frcp_rn(s);
+    }
+    float f[8];
+    bf16x8_to_f32(v, f);
+    quotients_for_codes<8>(f, s, z, kE4m3Low);
+    const uint32_t lo = f32x2_to_e4m3x2(f[0], f[1]) | (f32x2_to_e4m3x2(f[2], f[3]) << 16);
+    const uint32_t hi = f32x2_to_e4m3x2(f[4], f[5]) | (f32x2_to_e4m3x2(f[6], f[7]) << 16);
+    reinterpret_cast<uint2*>(out)[i] = make_uint2(lo, hi);
+  }
+}
+
 __global__ void __launch_bounds__(256) encode_prob_kernel(const float* p, uint8_t* out, size_t n,
                                                           float y, float z, int fast) {
   const size_t stride = (size_t)gridDim.x * blockDim.x;
@@ -295,6 +318,25 @@ cudaError_t launch_encode_prob(const float* p, uint8_t* out, size_t n, float pro
   size_t want = (n + 255) / 256;
   unsigned blocks = (unsigned)(want < (size_t)sms * 16 ? want : (size_t)sms * 16);
   encode_prob_kernel<<<blocks, 256, 0, st>>>(p, out, n, prob_scale, prob_recip, prob_fast);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq
+
+namespace kvq {
+
+cudaError_t launch_quantize_fp8(const uint16_t* x, size_t n, float scale, float recip,
+                                const float* head_scale, int head_len, int num_heads,
+                                uint8_t* out, cudaStream_t st) {
+  const size_t n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  size_t want = (n8 + 255) / 256;
+  unsigned blocks = (unsigned)(want < (size_t)sms * 16 ? want : (size_t)sms * 16);
+  quantize_fp8_kernel<<<blocks, 256, 0, st>>>(x, n8, scale, recip, head_scale, head_len,
+                                               num_heads, out);
   return cudaGetLastError();
 }
 

@@ -122,6 +122,27 @@ __device__ __forceinline__ void k_frag(uint32_t boxK, uint32_t boxKs, int row, i
 }
 
 // ---------------------------------------------------------------------------
+// Raw FP8 K codes for the E4M3 x E4M3 score MMA (m16n8k32; FP8 query): lane
+// (g, t) takes the D/4 code bytes (D/4) t .. of token row `row` as D/16
+// words, unconverted.  Word 2j feeds the k-columns 4t..4t+3 of k-step j
+// (head dims (D/4) t + 8j .. +3), word 2j + 1 the columns 4t+16..19 (dims
+// (D/4) t + 8j + 4 .. +7); the FP8 query is loaded with the same mapping.
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void k_raw_fp8(uint32_t boxK, int row, int t, uint32_t (&w)[D / 16]) {
+  using Gm = Geom<kFmtFp8, D>;
+  constexpr int NCH = D / 64;   // 16-byte chunks per lane per row
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    const uint4 v = lds128(boxK + row * Gm::kRow + (Gm::swz(row, t * NCH + i) << 4));
+    w[4 * i + 0] = v.x;
+    w[4 * i + 1] = v.y;
+    w[4 * i + 2] = v.z;
+    w[4 * i + 3] = v.w;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // V^T fragments (A operand of O^T = V^T P^T) for the box's 16 tokens:
 // a[i][0..3] for m-tile i.  Lane (g, t) covers tokens 2t, 2t+1 (a0, a1) and
 // 2t+8, 2t+9 (a2, a3); m-tile i, row g is value dim (D/8) g + 2 i and row

@@ -147,6 +147,21 @@ __device__ __forceinline__ float ex2(float x) {
   return r;
 }
 
+// D(16x8,f32) += A(16x32) * B(32x8) on E4M3 codes (products exact, fp32
+// accumulation).  Fragments of 8-bit elements, 4 per register:
+//   A: a0 = (row g, cols 4t..4t+3)   a1 = (row g+8, cols 4t..4t+3)
+//      a2 = (row g, cols 4t+16..19)  a3 = (row g+8, cols 4t+16..19)
+//   B: b0 = (rows 4t..4t+3, col g)   b1 = (rows 4t+16..19, col g)
+//   C: as for m16n8k16.
+__device__ __forceinline__ void mma_e4m3(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ void mma_bf16(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
   asm(

@@ -17,7 +17,7 @@ constexpr int kFmtNvfp4 = 2;
 constexpr int kBoxTokens = 16;    // tokens per TMA box (one 16-token page) = one MMA k-tile
 constexpr int kDecodeWarps = 4;   // each warp streams and consumes its own boxes
 constexpr int kDecodeThreads = 32 * kDecodeWarps;
-constexpr int kStages = 4;        // boxes in flight per warp
+constexpr int kStages = 3;        // boxes in flight per warp (3 measured equal or faster than 4)
 constexpr int kMaxGroup = 16;     // query heads per kv head (two 8-head MMA tiles)
 constexpr int kScoreCapacity = 16384;  // fp32 scores per CTA in FP8-prob mode
 constexpr int kPageCache = 512;   // block-table entries of a chunk kept in shared memory
@@ -43,7 +43,7 @@ struct AppendArgs {
 };
 
 struct PartialArgs {
-  const uint16_t* q;          // [B][Hq][Dqk] bf16
+  const void* q;              // [B][Hq][Dqk] bf16, or E4M3 codes when q_fp8
   const uint8_t* k_bscale;    // NVFP4 block scales (1-D bulk copies)
   const uint8_t* v_bscale;
   const uint16_t* k_pe;       // MLA rope keys
@@ -57,6 +57,9 @@ struct PartialArgs {
   int score_floats;           // FP8-prob mode: scores one chunk needs (<= kScoreCapacity)
   float qk_scale_log2;        // sm_scale * k_scale * log2(e)
   float sm_scale;             // with per-kv-head scales: the kernel forms the above per head
+  int q_fp8;                  // 1: q holds E4M3 codes (FP8 query)
+  float q_scale;              // FP8 query: dequantized q = code * q_scale
+  const float* q_hs;          // FP8 query: per-query-head scales (replace q_scale) or null
   const float* k_hs;          // per-kv-head scales (replace k_scale, v_scale) or null
   const float* v_hs;
   float pe_scale_log2;        // MLA rope part: sm_scale * log2(e)
@@ -65,6 +68,7 @@ struct PartialArgs {
   float prob_recip;           // RN(1 / prob_scale), used when prob_fast
   int prob_fast;              // 1: p / prob_scale by the reciprocal and one correction
   int fresh;                  // > 0: only the last `fresh` positions wait for the append
+  int q_len;                  // prefill: new query tokens per request
   // fused combine (kvq_decode): arrival counters [B * Hkv] and the output
   uint32_t* counters;         // null: partials only
   void* out;
@@ -101,6 +105,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_amax_bf16(const uint16_t* x, size_t n, float* out, cudaStream_t st);
 cudaError_t launch_encode(int kind, const float* x, uint8_t* out, size_t n, cudaStream_t st);
+// E4M3(fl32(x / s)) of bf16 x, s per tensor (recip = RN(1/s)) or per head
+cudaError_t launch_quantize_fp8(const uint16_t* x, size_t n, float scale, float recip,
+                                const float* head_scale, int head_len, int num_heads,
+                                uint8_t* out, cudaStream_t st);
 // E4M3(fl32(p / prob_scale)) per element, through the decode kernel's division
 cudaError_t launch_encode_prob(const float* p, uint8_t* out, size_t n, float prob_scale,
                                float prob_recip, int prob_fast, cudaStream_t st);
@@ -111,9 +119,13 @@ struct TensorMaps {
 
 cudaError_t launch_partial(int fmt, int D, bool probq, const TensorMaps& m, const PartialArgs& a,
                            cudaStream_t st);
+cudaError_t launch_partial_nvfp4(int D, bool probq, const TensorMaps& m, const PartialArgs& a,
+                                 cudaStream_t st);
 cudaError_t launch_mla_partial(const CUtensorMap& tcodes, const CUtensorMap& tpe,
                                const CUtensorMap& tcodes64, const CUtensorMap& tpe64,
                                const PartialArgs& a, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
+cudaError_t launch_prefill(int fmt, int D, const TensorMaps& m, const PartialArgs& a,
+                           cudaStream_t st);
 
 }  // namespace kvq

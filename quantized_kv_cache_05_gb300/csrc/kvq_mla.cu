@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // all of a thread's loads first: after an L2 flush each is a DRAM trip
       constexpr int kQItems = kMlaHeads * (kMlaQkDim / 8);
       constexpr int kQPer = (kQItems + kDecoders - 1) / kDecoders;
-      const uint16_t* qg = a.q + (size_t)b * kMlaHeads * kMlaQkDim;
+      const uint16_t* qg = static_cast<const uint16_t*>(a.q) + (size_t)b * kMlaHeads * kMlaQkDim;
       uint4 qv[kQPer];
 #pragma unroll
       for (int k = 0; k < kQPer; ++k) {

@@ -47,7 +47,7 @@ class kvq_decode_params(ctypes.Structure):
         ("batch", _i32), ("num_q_heads", _i32), ("qk_dim", _i32), ("v_dim", _i32),
         ("num_splits", _i32), ("seq_lens", _P), ("max_kv_len", _i32), ("sm_scale", _f),
         ("prob_scale", _f), ("out_dtype", _i32), ("out_scale", _f), ("error_flag", _P),
-        ("fresh_tokens", _i32),
+        ("fresh_tokens", _i32), ("q_fp8", _i32), ("q_scale", _f), ("q_head_scale", _P),
     ]
 
 
@@ -69,6 +69,9 @@ SIGNATURES = {
     "kvq_encode_e4m3": (_int, [_P, _P, _sz, _P]),
     "kvq_encode_e2m1": (_int, [_P, _P, _sz, _P]),
     "kvq_encode_prob_e4m3": (_int, [_P, _P, _sz, _f, ctypes.POINTER(_int), _P]),
+    "kvq_quantize_fp8": (_int, [_P, _sz, _f, _P, _int, _int, _P, _P]),
+    "kvq_prefill": (_int, [ctypes.POINTER(kvq_cache), ctypes.POINTER(kvq_decode_params), _int,
+                           _P, _P, _P]),
 }
 
 _lock = threading.Lock()
@@ -205,3 +208,17 @@ def kvq_encode_prob_e4m3(p, out, n: int, prob_scale: float, stream=None) -> tupl
     st = lib().kvq_encode_prob_e4m3(_addr(p), _addr(out), n, prob_scale, ctypes.byref(used),
                                     _stream(stream))
     return st, int(used.value)
+
+
+def kvq_quantize_fp8(x, n: int, scale: float, head_scale, head_len: int, num_heads: int, out,
+                     stream=None) -> int:
+    """E4M3 codes of bf16 x with a per-tensor scale or per-head scales."""
+    return lib().kvq_quantize_fp8(_addr(x), n, scale, _addr(head_scale), head_len, num_heads,
+                                  _addr(out), _stream(stream))
+
+
+def kvq_prefill(cache: kvq_cache, params: kvq_decode_params, q_len: int, q, out,
+                stream=None) -> int:
+    """Causal prefill attention of q_len new tokens per request (no KV split)."""
+    return lib().kvq_prefill(_ref(cache), _ref(params), q_len, _addr(q), _addr(out),
+                             _stream(stream))

@@ -105,6 +105,11 @@ class DecodeConfig:
     # > 0: the call right before on the stream is the append of the last
     # fresh_tokens positions, and the decode overlaps with it (kvq_decode_params)
     fresh_tokens: int = 0
+    # FP8 query: q holds E4M3 codes, dequantized with q_scale or the per-head
+    # q_head_scale tensor (float32 [num_q_heads] on the device)
+    q_fp8: bool = False
+    q_scale: float = 1.0
+    q_head_scale: Optional[torch.Tensor] = None
 
     def params(self, seq_lens: torch.Tensor, error_flag: Optional[torch.Tensor] = None
                ) -> kvq.kvq_decode_params:
@@ -117,6 +122,9 @@ class DecodeConfig:
         p.out_dtype, p.out_scale = OUT[self.out], self.out_scale
         p.error_flag = error_flag.data_ptr() if error_flag is not None else None
         p.fresh_tokens = self.fresh_tokens
+        p.q_fp8 = 1 if self.q_fp8 else 0
+        p.q_scale = self.q_scale
+        p.q_head_scale = self.q_head_scale.data_ptr() if self.q_head_scale is not None else None
         return p
 
 
@@ -173,3 +181,16 @@ def decode(cache: QuantizedKVCache, q: torch.Tensor, seq_lens: torch.Tensor, cfg
     kvq.check(kvq.kvq_decode_combine(p, ws.part_o, ws.part_lse, ws.out, stream),
               "kvq_decode_combine")
     return ws.out
+
+
+def prefill(cache: QuantizedKVCache, q: torch.Tensor, seq_lens: torch.Tensor, cfg: DecodeConfig,
+            q_len: int, out: Optional[torch.Tensor] = None,
+            error_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal prefill attention of q_len new tokens per request (kvq_prefill):
+    q bf16 [batch][q_len][Hq][D] -> out [batch][q_len][Hq][D]."""
+    if out is None:
+        out = torch.empty((cfg.batch, q_len, cfg.num_q_heads, cfg.v_dim), dtype=OUT_TORCH[cfg.out],
+                          device=q.device)
+    p = cfg.params(seq_lens, error_flag)
+    kvq.check(kvq.kvq_prefill(cache.struct(), p, q_len, q, out, stream), "kvq_prefill")
+    return out

@@ -165,6 +165,7 @@ class Workload:
     permute_pages: bool = False
     head_scales: bool = False     # per-kv-head static scales ("attn_head" strategy)
     head_exp: tuple = ()          # K/V of kv head h times 2^head_exp[h % len] (exact)
+    q_fp8: bool = False           # FP8 query (E4M3 codes with a per-tensor scale)
 
     @property
     def mla(self) -> bool:
@@ -313,6 +314,15 @@ def gqa_fp8_head_scales(L: int = 8192) -> Workload:
     w = gqa_fp8(L)
     w.name = f"gqa_fp8_head_L{L}"
     w.head_scales = True
+    return w
+
+
+def gqa_fp8_query(L: int = 8192) -> Workload:
+    """The GQA FP8 workload with an FP8 query (compressed-tensors PR 436
+    "QKV-FP8-Tensor": a static per-tensor query scale from its amax)."""
+    w = gqa_fp8(L)
+    w.name = f"gqa_fp8_q8_L{L}"
+    w.q_fp8 = True
     return w
 
 
