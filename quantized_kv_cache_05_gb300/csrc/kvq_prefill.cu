@@ -10,8 +10,12 @@
 //
 // GB300 design.  A CTA takes 64 query rows (row = query token * G + head of
 // one kv head) -- 16 per consumer warp -- of one (request, kv head); a fifth
-// warp streams the 16-token K/V boxes with TMA into a 4-stage ring that all
-// consumer warps read (full/empty mbarriers).  Per box and warp, on mma.sync
+// warp streams the 16-token K/V boxes with TMA into a 4-stage ring that the
+// consumer warps read (full/empty mbarriers).  A tile with fewer than four
+// 16-row groups (few new tokens, e.g. one: the decode shape) lends its idle
+// warps to the keys: with nrg row groups, nkg = 4 / nrg warps share each
+// group's rows and take every nkg-th box, and their softmax states are merged
+// through shared memory at the end.  Per box and warp, on mma.sync
 // m16n8k16 (f16 operands, fp32 accumulation):
 //   S = Q K^T   A = Q (16 rows, head dims permuted per lane like the K
 //               fragments), B = K^T from the decoded K box (k_frag), two
@@ -57,14 +61,16 @@ __global__ void __launch_bounds__(kPfThreads)
   const int bh = blockIdx.y, b = bh / a.Hkv, h = bh % a.Hkv;
   const int R = a.q_len * a.G;                  // query rows of the request
   const int r0 = blockIdx.x * kPfRows;          // first row of this tile
-  const int nact = min(kPfConsumers, (R - r0 + 15) / 16);   // consumer warps with rows
+  const int nrg = min(kPfConsumers, (R - r0 + 15) / 16);   // 16-row groups with rows
+  const int nkg = kPfConsumers / nrg;           // warps sharing a row group's keys
+  const int nact = nrg * nkg;                   // consumer warps at work
   const uint32_t ring = (smem_u32(dyn_smem) + 1023u) & ~1023u;
 
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
     for (int i = 0; i < kPfStages; ++i) {
       mbar_init(smem_u32(&sm.full[i]), 1);
-      mbar_init(smem_u32(&sm.empty[i]), nact);
+      mbar_init(smem_u32(&sm.empty[i]), nrg);   // each box has nrg consumers
     }
     fence_barrier_init();
   }
@@ -145,12 +151,13 @@ __global__ void __launch_bounds__(kPfThreads)
   const float qk_scale_log2 =
       a.k_hs ? (a.sm_scale * __ldg(a.k_hs + h)) * 1.4426950408889634f : a.qk_scale_log2;
   const float out_mult = a.v_hs ? __ldg(a.v_hs + h) : a.out_mult;
-  // rows of this lane: g and g + 8 of the warp's 16
+  const int rg = warp % nrg, kgi = warp / nrg;   // row group, key group
+  // rows of this lane: g and g + 8 of the group's 16
   int qi[2], qh[2], pos[2];
   bool rv[2];
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
-    const int row = r0 + 16 * warp + g + 8 * e;
+    const int row = r0 + 16 * rg + g + 8 * e;
     rv[e] = row < R;
     qi[e] = rv[e] ? row / a.G : 0;      // query token
     qh[e] = rv[e] ? row % a.G : 0;      // head within the kv head's group
@@ -195,7 +202,7 @@ __global__ void __launch_bounds__(kPfThreads)
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
   bool aborted = false;
 
-  for (int j = 0; j < nboxes; ++j) {
+  for (int j = kgi; j < nboxes; j += nkg) {
     const int st = j % kPfStages;
     bool got = true;
     if (lane == 0) got = wait_or_abort(smem_u32(&sm.full[st]), (j / kPfStages) & 1, abort_flag);
@@ -298,6 +305,46 @@ __global__ void __launch_bounds__(kPfThreads)
     record_error(a.error_flag, 1);
   }
 
+  // key groups 1.. of a row group hand their states (O fragments, m, lane
+  // sums l) to key group 0 through shared memory, which rescales to the
+  // common max and adds them
+  if (nkg > 1) {
+    float4* xo = reinterpret_cast<float4*>(dyn_smem + (ring - smem_u32(dyn_smem)) +
+                                           kPfStages * Gm::kStage);
+    const int slot_f4 = NT * 32 + 32;   // O fragments, then (m0, m1, l0, l1) per lane
+    if (kgi > 0) {
+      float4* my = xo + ((kgi - 1) * nrg + rg) * slot_f4;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) my[n * 32 + lane] = make_float4(o[n][0], o[n][1], o[n][2], o[n][3]);
+      my[NT * 32 + lane] = make_float4(m[0], m[1], l[0], l[1]);
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(nact * 32) : "memory");
+    if (kgi > 0) return;
+#pragma unroll 1
+    for (int k = 1; k < nkg; ++k) {
+      const float4* ot = xo + ((k - 1) * nrg + rg) * slot_f4;
+      const float4 ml = ot[NT * 32 + lane];
+      const float mo[2] = {ml.x, ml.y}, lo[2] = {ml.z, ml.w};
+      float fa[2], fb[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float M = fmaxf(m[r], mo[r]);
+        fa[r] = M == -INFINITY ? 0.f : ex2(m[r] - M);
+        fb[r] = M == -INFINITY ? 0.f : ex2(mo[r] - M);
+        l[r] = l[r] * fa[r] + lo[r] * fb[r];
+        m[r] = M;
+      }
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const float4 v = ot[n * 32 + lane];
+        o[n][0] = o[n][0] * fa[0] + v.x * fb[0];
+        o[n][1] = o[n][1] * fa[0] + v.y * fb[0];
+        o[n][2] = o[n][2] * fa[1] + v.z * fb[1];
+        o[n][3] = o[n][3] * fa[1] + v.w * fb[1];
+      }
+    }
+  }
+
   // normalize and store: accumulator (row g or g + 8, columns 2t, 2t+1) of
   // n-tile (i, c) is value dim (D/8)(2t + q) + 2i + c for column 2t + q
 #pragma unroll
@@ -308,6 +355,7 @@ __global__ void __launch_bounds__(kPfThreads)
     l[r] = v;
   }
   const float fac[2] = {l[0] > 0.f ? out_mult / l[0] : 0.f, l[1] > 0.f ? out_mult / l[1] : 0.f};
+  const bool bad = aborted || *abort_flag != 0;   // any warp of the CTA gave up
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     if (!rv[r]) continue;
@@ -318,7 +366,7 @@ __global__ void __launch_bounds__(kPfThreads)
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         const int dim = (D / 8) * (2 * t + q) + 2 * i + c;
-        const float val = aborted ? NAN : o[n][2 * r + q] * fac[r];
+        const float val = bad ? NAN : o[n][2 * r + q] * fac[r];
         if (a.out_dtype == 0) store_out_t<0>(a.out, a.out_scale, orow + dim, val);
         else if (a.out_dtype == 1) store_out_t<1>(a.out, a.out_scale, orow + dim, val);
         else store_out_t<2>(a.out, a.out_scale, orow + dim, val);
@@ -329,7 +377,10 @@ __global__ void __launch_bounds__(kPfThreads)
 
 template <int FMT, int D>
 cudaError_t launch_prefill_t(const TensorMaps& m, const PartialArgs& a, cudaStream_t st) {
-  const size_t smem = 1024 + (size_t)kPfStages * Geom<FMT, D>::kStage;
+  // ring, plus the state exchange of the key groups (up to three O
+  // fragment sets of 16 rows with their max and sums)
+  const size_t xbytes = (size_t)(kPfConsumers - 1) * ((D / 8) * 32 + 32) * 16;
+  const size_t smem = 1024 + (size_t)kPfStages * Geom<FMT, D>::kStage + xbytes;
   auto kern = prefill_kernel<FMT, D>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
