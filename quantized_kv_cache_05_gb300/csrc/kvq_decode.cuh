@@ -48,6 +48,8 @@
 
 #pragma once
 
+#include <algorithm>
+
 #include "kvq_attn.cuh"
 
 namespace kvq {
@@ -608,10 +610,16 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
   // fused combine: the G rows' partials staged at the ring base (the O
   // fragments are written out), the weights at the ring end
   if (a.counters) {
+    // staging area: everything from the ring base to the end of the dynamic
+    // shared memory (the launcher sizes it for the call's partials when the
+    // SM's residency allows), the weights at its end
     constexpr uint32_t kWbuf = (kMaxGroup * kMaxFusedSplits + kMaxGroup) * 4;
+    uint32_t dyn_bytes;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
+    const uint32_t usable = dyn_bytes - (ring - smem_u32(dyn_smem));
     fused_combine_staged<ctas_per_sm<FMT, D, PROBQ, NH>() == 4 ? 16 : 32>(
-        a, bh, part_row, a.G, ring, reinterpret_cast<const float*>(ofrag), Rg::kBytes - kWbuf,
-        reinterpret_cast<float*>(dyn_smem + (ring - smem_u32(dyn_smem)) + Rg::kBytes - kWbuf),
+        a, bh, part_row, a.G, ring, reinterpret_cast<const float*>(ofrag), usable - kWbuf,
+        reinterpret_cast<float*>(dyn_smem + (ring - smem_u32(dyn_smem)) + usable - kWbuf),
         smem_u32(&sm.comb_full));
   }
 }
@@ -620,7 +628,18 @@ template <int FMT, int D, bool PROBQ, int NH, bool QF8>
 cudaError_t launch_partial_t(const TensorMaps& m, const PartialArgs& a, cudaStream_t st) {
   using Rg = Ring<FMT, D, PROBQ, NH>;
   static_assert(Rg::kBytes >= Rg::kEpilogue && Rg::kBytes >= Rg::kStream, "ring too small");
-  const size_t smem = 1024 + (size_t)Rg::kBytes + (PROBQ ? (size_t)a.score_floats * 4 : 0);
+  size_t smem = 1024 + (size_t)Rg::kBytes + (PROBQ ? (size_t)a.score_floats * 4 : 0);
+  if (a.counters) {
+    // room for the fused merge to stage its partials (G rows x s splits x Dv
+    // floats, and the weights) in one bulk copy, within the shared memory
+    // that keeps ctas_per_sm CTAs resident (228 KB per SM, 1 KB reserved per
+    // CTA, the static part under 4 KB, the alignment slack)
+    constexpr size_t kPerCta = 233472 / ctas_per_sm<FMT, D, PROBQ, NH>() - 1024 - 4096 - 1024;
+    const size_t need = 1024 + (size_t)a.G * a.num_splits * a.Dv * 4 +
+                        (kMaxGroup * kMaxFusedSplits + kMaxGroup) * 4;
+    smem = std::max(smem, std::min(need, kPerCta));
+  }
+  smem = (smem + 15) / 16 * 16;
   auto kern = partial_kernel<FMT, D, PROBQ, NH, QF8>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
