@@ -403,6 +403,52 @@ __device__ __forceinline__ void merge_rows(const float* __restrict__ part_o,
                            out_scale);
 }
 
+// Weighted sum of cnt staged splits of one (row, 4 value dims) item: p points
+// at the item's first split, consecutive splits nq float4 apart; wr holds the
+// splits' weights.  The loads run four splits ahead, the adds stay in split
+// order (the same sums, bit for bit, as the global-memory merge).
+__device__ __forceinline__ float4 accum_splits(const float4* p, int nq, const float* wr, int cnt,
+                                               float4 acc) {
+  int j = 0;
+#pragma unroll 1
+  for (; j + 4 <= cnt; j += 4) {
+    float4 v[4];
+    float wj[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[k] = p[(size_t)(j + k) * nq];
+      wj[k] = wr[j + k];
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc.x += wj[k] * v[k].x;
+      acc.y += wj[k] * v[k].y;
+      acc.z += wj[k] * v[k].z;
+      acc.w += wj[k] * v[k].w;
+    }
+  }
+#pragma unroll 1
+  for (; j < cnt; ++j) {
+    const float4 v = p[(size_t)j * nq];
+    const float wj = wr[j];
+    acc.x += wj * v.x;
+    acc.y += wj * v.y;
+    acc.z += wj * v.z;
+    acc.w += wj * v.w;
+  }
+  return acc;
+}
+
+template <int DT>
+__device__ __forceinline__ void store_item(const PartialArgs& a, size_t row0, int r, int d4,
+                                           float4 acc, float iv) {
+  const size_t o = (row0 + r) * a.Dv + 4 * d4;
+  store_out_t<DT>(a.out, a.out_scale, o + 0, acc.x * iv);
+  store_out_t<DT>(a.out, a.out_scale, o + 1, acc.y * iv);
+  store_out_t<DT>(a.out, a.out_scale, o + 2, acc.z * iv);
+  store_out_t<DT>(a.out, a.out_scale, o + 3, acc.w * iv);
+}
+
 // Staged merge: the s partials of rows [row0, row0 + rows) are contiguous in
 // global memory ([row][split][Dv] floats); with them in shared memory (one
 // bulk copy) the weighted sum is a short loop, four value dims per thread and
@@ -416,31 +462,21 @@ __device__ __forceinline__ void merge_staged(const PartialArgs& a, size_t row0, 
 #pragma unroll 1
   for (int i = threadIdx.x; i < rows * nq; i += blockDim.x) {
     const int r = i / nq, d4 = i % nq;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-    for (int j = 0; j < s; ++j) {
-      const float wj = w[r * kMaxFusedSplits + j];
-      const float4 v = po[(r * s + j) * nq + d4];
-      acc.x += wj * v.x;
-      acc.y += wj * v.y;
-      acc.z += wj * v.z;
-      acc.w += wj * v.w;
-    }
-    const float iv = ok ? winv[r] : NAN;
-    const size_t o = (row0 + r) * a.Dv + 4 * d4;
-    store_out_t<DT>(a.out, a.out_scale, o + 0, acc.x * iv);
-    store_out_t<DT>(a.out, a.out_scale, o + 1, acc.y * iv);
-    store_out_t<DT>(a.out, a.out_scale, o + 2, acc.z * iv);
-    store_out_t<DT>(a.out, a.out_scale, o + 3, acc.w * iv);
+    const float4 acc = accum_splits(po + (size_t)r * s * nq + d4, nq, w + r * kMaxFusedSplits, s,
+                                    make_float4(0.f, 0.f, 0.f, 0.f));
+    store_item<DT>(a, row0, r, d4, acc, ok ? winv[r] : NAN);
   }
 }
 
 // Fused combine with staging: the arrival protocol of fused_combine; the
 // last CTA brings its rows' partials into shared memory with one bulk copy
 // when they fit in `cap` bytes at `stage` (16-byte aligned, free), else it
-// runs the general merge.  The async-proxy read follows the acquire, behind
-// a proxy fence.  bar: an mbarrier initialized with one arrival and unused
-// so far; wbuf: kMaxGroup * (kMaxFusedSplits + 1) floats outside the stage.
+// runs the general merge from global memory.  (Splitting the copy into
+// rounds of a few splits per row was measured slower than the global merge:
+// the row pieces are separate bulk copies, each a full round trip.)  The
+// async-proxy read follows the acquire, behind a proxy fence.  bar: an
+// mbarrier initialized with one arrival and unused so far; wbuf: kMaxGroup *
+// (kMaxFusedSplits + 1) floats outside the stage.
 template <int DEPTH = 32, int NI = 1>
 __device__ __forceinline__ void fused_combine_staged(const PartialArgs& a, int bh, size_t part_row,
                                                      int rows, uint32_t stage, const float* stage_p,
@@ -472,8 +508,7 @@ __device__ __forceinline__ void fused_combine_staged(const PartialArgs& a, int b
     bulk_load(stage, a.part_o + part_row * s * a.Dv, (uint32_t)bytes, bar);
   }
   merge_weights(a.part_lse, part_row, rows, s, wbuf, winv);
-  const bool ok = mbar_wait(bar, 0);
-  __syncthreads();
+  const bool ok = __syncthreads_and(mbar_wait(bar, 0) ? 1 : 0) != 0;
   if (a.out_dtype == 0)
     merge_staged<0>(a, part_row, rows, stage_p, wbuf, winv, ok);
   else if (a.out_dtype == 1)

@@ -262,15 +262,33 @@ def gqa4k():
     return S, S.oracle_decode()[0]
 
 
-@pytest.mark.parametrize("s", [29, 30, 40, 64])
+@pytest.mark.parametrize("s", [29, 30, 32, 33, 40, 57, 64])
 def test_fused_many_splits(gqa4k, s):
-    """Up to 29 splits the last CTA stages the partials of its 4 heads (61 KB)
-    in shared memory; beyond that it merges from global memory.  Both paths
-    give the two-launch result (fp32 sums in the same split order)."""
+    """Up to 32 splits the last CTA stages the partials of its 4 heads (2 KB
+    a split) in shared memory with one copy; beyond that it merges from
+    global memory.  Both paths give the two-launch result (fp32 sums in the
+    same split order)."""
     S, ref = gqa4k
     a, _ = S.gpu_decode(s)
     b, ws = fused(S, s)
     assert_f32_close(b.cpu().numpy(), ref, f"fused s={s}")
+    assert torch.allclose(a, b, rtol=4e-7, atol=1e-7)
+    assert not ws.counters.any()
+
+
+@pytest.mark.parametrize("fmt,s", [("fp8", 13), ("fp8", 20), ("fp8", 47), ("nvfp4", 57)])
+def test_fused_many_splits_large_group(fmt, s):
+    """16 query heads per kv head: 8 KB of partials per split, so beyond 13
+    splits the last CTA merges from global memory with four heads' columns
+    per thread."""
+    w = synth.gqa_fp8(3000) if fmt == "fp8" else synth.nvfp4(3000)
+    w.B, w.Hq, w.Hkv = 2, 16, 1
+    w.seq_lens = np.array([3000, 1777], np.int32)
+    S = Setup(w)
+    ref, _ = S.oracle_decode()
+    a, _ = S.gpu_decode(s)
+    b, ws = fused(S, s)
+    assert_f32_close(b.cpu().numpy(), ref, f"fused G=16 {fmt} s={s}")
     assert torch.allclose(a, b, rtol=4e-7, atol=1e-7)
     assert not ws.counters.any()
 
