@@ -146,7 +146,9 @@ __device__ __forceinline__ void k_raw_fp8(uint32_t boxK, int row, int t, uint32_
 // V^T fragments (A operand of O^T = V^T P^T) for the box's 16 tokens:
 // a[i][0..3] for m-tile i.  Lane (g, t) covers tokens 2t, 2t+1 (a0, a1) and
 // 2t+8, 2t+9 (a2, a3); m-tile i, row g is value dim (D/8) g + 2 i and row
-// g + 8 is (D/8) g + 2 i + 1.  Invalid tokens read as zero codes.
+// g + 8 is (D/8) g + 2 i + 1.  Invalid tokens (rows past the chunk) give
+// zero: FP8 codes are zeroed, NVFP4 block scales are zeroed (every E2M1 code
+// is finite, so the products are zero).
 // ---------------------------------------------------------------------------
 template <int FMT, int D, int SSTRIDE = Geom<FMT, D>::kSRow>
 __device__ __forceinline__ void v_frag(uint32_t boxV, uint32_t boxVs, int t, int g, int nvalid,
@@ -165,10 +167,14 @@ __device__ __forceinline__ void v_frag(uint32_t boxV, uint32_t boxVs, int t, int
         uint2 v = lds64(boxV + tk[r] * 64 + (Gm::swz(tk[r], g >> 1) << 4) + ((g & 1) << 3));
         w[r][0] = v.x; w[r][1] = v.y;
       }
-      if (tk[r] >= nvalid) {
+    }
+    if (nvalid < kBoxTokens) {   // ragged box: rows past the chunk read as zero codes
 #pragma unroll
-        for (int k = 0; k < NW; ++k) w[r][k] = 0u;
-      }
+      for (int r = 0; r < 4; ++r)
+        if (tk[r] >= nvalid) {
+#pragma unroll
+          for (int k = 0; k < NW; ++k) w[r][k] = 0u;
+        }
     }
 #pragma unroll
     for (int k = 0; k < NW; ++k) {
@@ -208,12 +214,14 @@ __device__ __forceinline__ void v_frag(uint32_t boxV, uint32_t boxVs, int t, int
         sc[r][0] = s2 & 0xFFu;
         sc[r][1] = s2 >> 8;
       }
-      if (tk[r] >= nvalid) {
+    }
+    if (nvalid < kBoxTokens) {   // ragged box: rows past the chunk scale to zero
 #pragma unroll
-        for (int k = 0; k < NW; ++k) v[r][k] = 0u;
+      for (int r = 0; r < 4; ++r)
+        if (tk[r] >= nvalid) {
 #pragma unroll
-        for (int k = 0; k < NB; ++k) sc[r][k] = 0u;
-      }
+          for (int k = 0; k < NB; ++k) sc[r][k] = 0u;
+        }
     }
     uint32_t s01[NB], s89[NB];   // (scale of token 2t, 2t+1) and (2t+8, 2t+9)
 #pragma unroll

@@ -167,15 +167,28 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
   __syncthreads();
   volatile int* abort_flag = &sm.abort_flag;
 
-  // Issue the copies of this warp's j-th load (lane 0 only): load j covers
-  // box w + 4 (j % nw); in FP8-prob mode loads [0, nw) bring K, [nw, 2nw) V.
-  auto issue = [&](int j) {
-    const int sweep = PROBQ ? j / nw : 0;
+  // Issue the copies of this warp's j-th load (lane 0 only) into stage st:
+  // load j covers box w + 4 (j % nw); in FP8-prob mode loads [0, nw) bring
+  // K, [nw, 2nw) V.  Loads are issued in order; the page and in-page offset
+  // of the next one advance by 64 tokens per load (no division per box).
+  const int tok_first = cstart + warp * kBoxTokens;
+  int nx_pidx = tok_first / a.ps;
+  int nx_off = tok_first - nx_pidx * a.ps;
+  auto issue = [&](int j, int st) {
+    const int sweep = PROBQ ? (j >= nw ? 1 : 0) : 0;
     const int box = warp + kDecodeWarps * (j - sweep * nw);
     const bool loadK = !PROBQ || sweep == 0;
     const bool loadV = !PROBQ || sweep == 1;
-    const int tok = cstart + box * kBoxTokens;
-    const int pidx = tok / a.ps;
+    if (PROBQ && j == nw) {   // the V sweep starts over at the warp's first box
+      nx_pidx = tok_first / a.ps;
+      nx_off = tok_first - nx_pidx * a.ps;
+    }
+    const int pidx = nx_pidx, off = nx_off;
+    nx_off += kDecodeWarps * kBoxTokens;
+    while (nx_off >= a.ps) {
+      nx_off -= a.ps;
+      ++nx_pidx;
+    }
     int page;
     if (pidx - p0 < kPageCache) {
       page = sm.pages[pidx - p0];
@@ -186,12 +199,11 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
         page = 0;
       }
     }
-    const long row = ((long)page * a.Hkv + h) * a.ps + (tok % a.ps);
+    const long row = ((long)page * a.Hkv + h) * a.ps + off;
     if (!dep_done && box >= fresh_box) {
       griddep_wait();
       dep_done = true;
     }
-    const int st = j % kStages;
     const uint32_t full = smem_u32(&sm.full[warp][st]);
     const uint32_t sbase = ring + (warp * kStages + st) * Rg::kStageBytes;
     const uint32_t bytes = (loadK ? Gm::kBoxK + Gm::kBoxS : 0) + (loadV ? Gm::kBoxK + Gm::kBoxS : 0);
@@ -215,7 +227,7 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
   int issued = 0;
   if (lane == 0) {
 #pragma unroll 1   // one copy of the issue code (it runs cold, once per CTA)
-    for (; issued < min(total, kStages); ++issued) issue(issued);
+    for (; issued < min(total, kStages); ++issued) issue(issued, issued);
   }
 
   const int hq0 = h * a.G;
@@ -306,14 +318,13 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
   for (int hh = 0; hh < NH; ++hh) m[hh][0] = m[hh][1] = -INFINITY, l[hh][0] = l[hh][1] = 0.f;
   bool aborted = false;
 
+  int st = 0;          // stage of the current load
+  uint32_t phase = 0;  // its mbarrier phase parity
   for (int sweep = 0; sweep < kSweeps; ++sweep) {
     for (int jj = 0; jj < nw && !aborted; ++jj) {
-      const int j = sweep * nw + jj;
-      const int st = j % kStages;
       // one lane polls the barrier; the vote tells the warp the outcome
       bool got = true;
-      if (lane == 0)
-        got = wait_or_abort(smem_u32(&sm.full[warp][st]), (j / kStages) & 1, abort_flag);
+      if (lane == 0) got = wait_or_abort(smem_u32(&sm.full[warp][st]), phase, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         aborted = true;
         break;
@@ -490,7 +501,11 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
       __syncwarp();
       if (lane == 0 && issued < total) {
         fence_proxy_async_shared();   // generic reads of the stage before the async overwrite
-        issue(issued++);
+        issue(issued++, st);
+      }
+      if (++st == kStages) {
+        st = 0;
+        phase ^= 1u;
       }
     }
     if constexpr (PROBQ) {
