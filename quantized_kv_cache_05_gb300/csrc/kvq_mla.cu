@@ -11,31 +11,34 @@
 // k_pe the bf16 rope key (64 wide).  The split-KV scheme is the GQA kernel's
 // (Model-Optimizer PR 1832 notes).
 //
-// GB300 design.  One CTA per SM runs one chunk in tiles of 64 tokens with
+// GB300 design.  One CTA per SM runs one chunk in tiles of 128 tokens with
 // warp-specialized roles that hand work over through mbarriers:
-//  * TMA copies stream each tile's latent codes (128-byte swizzled boxes),
-//    block scales (1-D bulk copy) and rope keys into a two-stage ring; lane 0
-//    of the last decode warp issues them when a stage has been decoded;
-//  * eight decode warps turn a tile, once, into an f16 [token][dim] tile
+//  * TMA copies bring a tile's latent codes (128-byte swizzled boxes) and
+//    block scales (1-D bulk copies) into a raw buffer, and its rope keys
+//    straight into one of two bf16 operand tiles (the same swizzled layout);
+//    lane 0 of the last decode warp issues them once the previous tile has
+//    been decoded;
+//  * six decode warps turn the tile, once, into an f16 [token][dim] tile
 //    (E2M1 x E4M3 -> f16 is exact) in the 128-byte-swizzled layout that is
 //    the K-major A operand of S^T = K Q^T and, read MN-major, the A operand
-//    of O^T = V^T P^T; they copy the rope keys into a bf16 operand tile;
-//  * the MMAs are tcgen05.mma (kind::f16, M = 128, N = 16 heads): S^T of the
-//    latent (f16) and of the rope part (bf16) into two tensor-memory
-//    accumulators (their scales differ), and O^T of four 128-dim blocks into
-//    a third.  One thread issues S^T once a tile is decoded, another O^T once
-//    its P^T is written, so that one's wait and fence overlap the other's
-//    batch;
-//  * two softmax warps read S^T from tensor memory (one token per thread,
-//    all 16 heads), run the softmax with a lazily moving reference max and
-//    write P^T (f16) as the B operand of the O^T MMA.  When the reference
-//    max moves, O is rescaled in tensor memory by the four warps of the
-//    four lane sub-partitions (the softmax warps and decode warps 2-3).
-// Decoded tiles, rope tiles, S^T accumulators and P^T are double buffered.
-// The M = 128 S^T MMA over a 64-token tile also computes 64 rows from the
-// shared memory after the tile (always inside the allocation); they land in
-// tensor-memory lanes 64..127, which are never read.  Every wait is bounded;
-// a timeout sets an error bit and the partials become NaN.
+//    of O^T = V^T P^T.  They decode it one 128-dim block at a time, each
+//    block as soon as the O^T MMAs of the previous tile have finished
+//    reading that block, so that decoding overlaps the tensor pipe;
+//  * the MMAs are tcgen05.mma (kind::f16, M = 128 tokens or value dims,
+//    N = 16 heads): S^T of the latent (f16) block by block as the blocks are
+//    decoded and of the rope part (bf16) into two tensor-memory accumulators
+//    (their scales differ), and O^T of four 128-dim blocks into a third,
+//    each block committed on its own barrier.  One thread issues S^T,
+//    another O^T;
+//  * four softmax warps (one per tensor-memory lane quarter) read S^T (one
+//    token per thread, all 16 heads), run the softmax with a lazily moving
+//    reference max, rescale O in tensor memory when it moves and write P^T
+//    (f16) as the B operand of the O^T MMA.
+// A 128-token tile fills the M = 128 rows of every S^T MMA (a 64-token tile
+// left half of them empty): 68 MMAs per 128 tokens instead of 104.  The
+// f16 tile is single buffered; rope tiles, S^T accumulators and P^T are
+// double buffered.  Every wait is bounded; a timeout sets an error bit and
+// the partials become NaN.
 
 #include "kvq_attn.cuh"
 
@@ -46,64 +49,60 @@ constexpr int kMlaLat = 512;
 constexpr int kMlaRope = 64;
 constexpr int kMlaHeads = 16;
 constexpr int kMlaQkDim = kMlaLat + kMlaRope;
-constexpr int kT = 64;              // tokens per tile
+constexpr int kT = 128;             // tokens per tile
 constexpr int kBoxes = kT / kBoxTokens;
-constexpr int kDecodeWarps = 8;     // decode warps 2..9 (2-3 also rescale O)
-constexpr int kDecoders = 32 * kDecodeWarps;
-constexpr int kWorkers = 64 + kDecoders;   // + softmax warps 0-1
-constexpr int kSWarp = kWorkers / 32, kOWarp = kSWarp + 1;   // TMA + S^T issue, O^T issue
+constexpr int kSoftWarps = 4;       // warps 0-3: softmax, one per lane quarter
+constexpr int kDecWarps = 6;        // warps 4-9: decode
+constexpr int kDecoders = 32 * kDecWarps;
+constexpr int kWorkers = 32 * kSoftWarps + kDecoders;
+constexpr int kSWarp = kWorkers / 32, kOWarp = kSWarp + 1;   // S^T issue, O^T issue
 constexpr int kThreads = kWorkers + 64;
+constexpr int kBlocks = kMlaLat / 128;   // 128-dim blocks (two 64-dim atom columns)
 constexpr int kTmemCols = 128;      // S lat [2] @0,16 | S rope [2] @32,48 | O^T 4 x 16 @64
 constexpr int kColSLat = 0, kColSPe = 32, kColO = 64;
 
 // shared-memory map (bytes from the 1024-aligned base); every MMA operand
 // tile starts on a 1024-byte boundary (the 128-byte swizzle period)
-constexpr int kTileBytes = kT * kMlaLat * 2;                  // f16 latent tile, 64 KB
-constexpr int kOffTile = 0;                                   // two tiles
-constexpr int kRawCodes = kT * kMlaLat / 2;                   // 16 KB: [half][64 rows x 128 B]
-constexpr int kRawScales = kT * (kMlaLat / 16);               // 2 KB block scales
-constexpr int kPeBytes = kT * kMlaRope * 2;                   // bf16 rope tile, 8 KB
-constexpr int kRawStage = kRawCodes + kRawScales + kPeBytes;  // codes | scales | rope keys
-constexpr int kRawStages = 2;
-constexpr int kOffRaw = kOffTile + 2 * kTileBytes;
-constexpr int kOffPe = kOffRaw + kRawStages * kRawStage;      // two rope operand tiles
+constexpr int kColBytes = kT * 128;                           // one 64-dim column, 16 KB
+constexpr int kTileBytes = kT * kMlaLat * 2;                  // f16 latent tile, 128 KB
+constexpr int kOffTile = 0;
+constexpr int kHalfBytes = kT * 128;                          // codes of 256 dims, 16 KB
+constexpr int kRawCodes = 2 * kHalfBytes;                     // [half][128 rows x 128 B]
+constexpr int kRawScales = kT * (kMlaLat / 16);               // 4 KB block scales
+constexpr int kOffRaw = kOffTile + kTileBytes;                // one raw tile
+constexpr int kPeBytes = kT * kMlaRope * 2;                   // bf16 rope tile, 16 KB
+constexpr int kOffPe = kOffRaw + kRawCodes + kRawScales;      // two rope operand tiles
 constexpr int kOffQLat = kOffPe + 2 * kPeBytes;               // f16 [16][512], 16 KB
 constexpr int kOffQPe = kOffQLat + kMlaHeads * kMlaLat * 2;   // bf16 [16][64], 2 KB
-constexpr int kPBytes = kMlaHeads * kT * 2;                   // f16 P^T [16][64], 2 KB
+constexpr int kPBytes = kMlaHeads * kT * 2;                   // f16 P^T [16][128], 4 KB
 constexpr int kOffP = kOffQPe + kMlaHeads * kMlaRope * 2;     // two P^T tiles
 constexpr int kSmemUsed = kOffP + 2 * kPBytes;
 constexpr int kSmemBytes = kSmemUsed + 1024;                  // alignment slack
-static_assert(kRawStage % 1024 == 0 && (kRawCodes + kRawScales) % 1024 == 0 && kOffPe % 1024 == 0 && kOffQLat % 1024 == 0 &&
-                  kOffQPe % 1024 == 0 && kOffP % 1024 == 0,
+static_assert(kOffRaw % 1024 == 0 && (kOffRaw + kRawCodes) % 1024 == 0 && kOffPe % 1024 == 0 &&
+                  kOffQLat % 1024 == 0 && kOffQPe % 1024 == 0 && kOffP % 1024 == 0,
               "operand tiles on the swizzle period");
-// the S^T MMA reads 128 rows (16 KB per 64-dim column of atoms) of a 64-row
-// tile: the extra 8 KB after the last tile and the last rope tile stay inside
-static_assert(kOffTile + 2 * kTileBytes + 8192 <= kSmemUsed, "tile over-read in bounds");
-static_assert(kOffPe + 2 * kPeBytes + 8192 <= kSmemUsed, "rope over-read in bounds");
-static_assert(kRawStages * kRawStage >= kMaxGroup * (kMaxFusedSplits + 1) * 4,
-              "combine weights fit in the raw ring");
+static_assert(kRawCodes + kRawScales >= kMaxGroup * (kMaxFusedSplits + 1) * 4,
+              "combine weights fit in the raw buffer");
 
 struct MlaSmem {
-  uint64_t raw_full[kRawStages];   // codes, scales and rope keys of a tile landed
+  uint64_t raw_full;               // codes and scales of a tile landed
+  uint64_t pe_full[2];             // rope keys of a tile landed (per rope buffer)
+  uint64_t dec_blk[kBlocks];       // decode warps: 128-dim block of the tile written
   uint64_t s_done[2];              // S^T MMAs of a tile completed
-  uint64_t o_done[2];              // O^T MMAs of a tile completed
-  uint64_t dec_ready[2];           // decode warps: tile decoded (operands visible)
-  uint64_t p_done[2];              // softmax warps: P^T and the rescale decision written
-  uint64_t p_ready[2];             // P^T written and O rescaled: O^T MMA may go
-  uint64_t resc_done;              // warps 2-3: their half of an O rescale is done
+  uint64_t o_blk[kBlocks];         // O^T MMAs of a 128-dim block completed
+  uint64_t p_ready[2];             // P^T written and O rescaled: O^T MMAs may go
   uint64_t comb_full;              // fused combine: partials landed
   uint32_t tmem;                   // tensor-memory base address
   int abort_flag;
-  int rescale[2];                  // tile parity: O must be rescaled before O^T MMA t
-  int need[2];                     // softmax warps: the reference max must move
-  float alpha[2][kMlaHeads];       // tile parity: O rescale factors
-  float wmax[2][kMlaHeads];        // per-warp tile maxima
-  float lsum[2][kMlaHeads];        // per-warp denominators (end)
+  int need[kSoftWarps];            // softmax warps: the reference max must move
+  float wmax[kSoftWarps][kMlaHeads];   // per-warp tile maxima
+  float lsum[kSoftWarps][kMlaHeads];   // per-warp denominators (end)
   float m[kMlaHeads];              // final reference max (end)
   uint32_t qmax[kMlaHeads];        // largest |q_lat| per head (bf16 magnitude bits)
   float qfac[kMlaHeads];           // latent score scale per head (log2 domain)
   int pages[kPageCache];
 };
+static_assert(kSmemBytes + sizeof(MlaSmem) <= 232448, "shared memory of one CTA");
 
 // ----------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor: start, leading/stride byte offsets (16-byte
@@ -208,21 +207,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (smem_u32(dyn_smem) + 1023u) & ~1023u;
   uint8_t* gbase = dyn_smem + (base - smem_u32(dyn_smem));
   volatile int* abort_flag = &sm.abort_flag;
+  const int dt = tid - 32 * kSoftWarps;   // decode thread 0..kDecoders-1 (decode warps)
+  const bool decoder = dt >= 0 && dt < kDecoders;
 
   // ---- setup that reads no input: barriers, tensor memory
   if (tid == 0) {
-    for (int i = 0; i < kRawStages; ++i) mbar_init(smem_u32(&sm.raw_full[i]), 1);
+    mbar_init(smem_u32(&sm.raw_full), 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sm.pe_full[i]), 1);
       mbar_init(smem_u32(&sm.s_done[i]), 1);
-      mbar_init(smem_u32(&sm.o_done[i]), 1);
-      mbar_init(smem_u32(&sm.dec_ready[i]), kDecoders);
-      mbar_init(smem_u32(&sm.p_done[i]), 1);
       mbar_init(smem_u32(&sm.p_ready[i]), 1);
     }
-    mbar_init(smem_u32(&sm.resc_done), 64);
+    for (int i = 0; i < kBlocks; ++i) {
+      mbar_init(smem_u32(&sm.dec_blk[i]), kDecoders);
+      mbar_init(smem_u32(&sm.o_blk[i]), 1);
+    }
     mbar_init(smem_u32(&sm.comb_full), 1);
     sm.abort_flag = 0;
-    sm.rescale[0] = sm.rescale[1] = 0;
     for (int h = 0; h < kMlaHeads; ++h) sm.qmax[h] = 0u;
     fence_barrier_init();
     prefetch_tmap(&tmCodes);
@@ -240,6 +241,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   // overlap mode (a.fresh > 0): only loads of tiles holding the last a.fresh
   // positions wait for the preceding append
   if (a.fresh == 0) griddep_wait();
+
+  // Q (decode warps): every load first, before the block table, so that the
+  // two DRAM trips after an L2 flush overlap
+  constexpr int kQItems = kMlaHeads * (kMlaQkDim / 8);
+  constexpr int kQPer = (kQItems + kDecoders - 1) / kDecoders;
+  uint4 qv[kQPer];
+  if (decoder) {
+    const uint16_t* qg = static_cast<const uint16_t*>(a.q) + (size_t)b * kMlaHeads * kMlaQkDim;
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = dt + k * kDecoders;
+      if (i < kQItems)
+        qv[k] = *reinterpret_cast<const uint4*>(qg + (size_t)(i / (kMlaQkDim / 8)) * kMlaQkDim +
+                                                (i % (kMlaQkDim / 8)) * 8);
+    }
+  }
 
   // ---- chunk of this split
   int L = a.seq_lens[b];
@@ -289,81 +306,84 @@ __global__ void __launch_bounds__(kThreads, 1)
     return (long)page * a.ps + (tok % a.ps);
   };
 
-  // softmax state (warps 0, 1: one token per thread, all 16 heads)
-  float m[kMlaHeads], l[kMlaHeads];
-#pragma unroll
-  for (int h = 0; h < kMlaHeads; ++h) m[h] = -INFINITY, l[h] = 0.f;
-
   // Descriptors are built once; per MMA only the start-address field moves
   // (16-byte units, no carry out of 14 bits: every shared address is below
-  // 256 KB).  Both buffer parities are precomputed.
+  // 256 KB).
   const uint64_t dq = sdesc(base + kOffQLat, 16, 1024);
   const uint64_t dqpe = sdesc(base + kOffQPe, 16, 1024);
-  const uint64_t dk0 = sdesc(base + kOffTile, 16, 1024);   // K-major tile
-  const uint64_t dk1 = sdesc(base + kOffTile + kTileBytes, 16, 1024);
+  const uint64_t dk = sdesc(base + kOffTile, 16, 1024);   // K-major tile
 
-  // Copies of tile x into raw stage x % 2 (by lane 0 of the last decode
-  // warp).  A tile inside one page moves as four copies (64-row boxes),
-  // otherwise as four per 16-token box.  Stage layout: codes [half][row][128 B]
-  // (128-byte swizzle), scales [row][32 B], rope keys [row][128 B].
-  auto fresh_wait = [&](int x) {
+  // Copies of tile x (by lane 0 of the last decode warp): codes and scales
+  // into the raw buffer, rope keys into rope tile x % 2.  Each 64-token half
+  // inside one page moves as four copies (64-row boxes), otherwise as four
+  // per 16-token box.  Raw layout: codes [half][row][128 B] (128-byte
+  // swizzle), scales [row][32 B]; rope tile [row][128 B] (128-byte swizzle).
+  auto issue_raw = [&](int x) {
     if (!dep_done && x * kT + kT > fresh_tok) {
       griddep_wait();
       dep_done = true;
     }
-  };
-  auto issue_raw = [&](int x) {
-    fresh_wait(x);
     const int nb = min(kBoxes, (ntok - x * kT + kBoxTokens - 1) / kBoxTokens);
-    const uint32_t st = base + kOffRaw + (x % kRawStages) * kRawStage;
-    const uint32_t bar = smem_u32(&sm.raw_full[x % kRawStages]);
-    constexpr uint32_t kRowBytes = kMlaLat / 2 + kMlaLat / 16 + kMlaRope * 2;   // 416
-    mbar_arrive_expect_tx(bar, nb * kBoxTokens * kRowBytes);
-    const int tok0 = cstart + x * kT;
-    const long row0 = cache_row(tok0);
-    if (nb == kBoxes && tok0 / a.ps == (tok0 + kT - 1) / a.ps) {
-      tma_load_3d(st, &tmCodes64, 0, 0, (int)row0, bar);
-      tma_load_3d(st + kRawCodes / 2, &tmCodes64, 0, 1, (int)row0, bar);
-      bulk_load(st + kRawCodes, a.k_bscale + row0 * (kMlaLat / 16), kT * (kMlaLat / 16), bar);
-      tma_load_2d(st + kRawCodes + kRawScales, &tmPe64, 0, (int)row0, bar);
-      return;
-    }
-    for (int k = 0; k < nb; ++k) {
-      const long row = k == 0 ? row0 : cache_row(tok0 + k * kBoxTokens);
-      tma_load_3d(st + k * 2048, &tmCodes, 0, 0, (int)row, bar);
-      tma_load_3d(st + kRawCodes / 2 + k * 2048, &tmCodes, 0, 1, (int)row, bar);
-      bulk_load(st + kRawCodes + k * (kBoxTokens * (kMlaLat / 16)),
-                a.k_bscale + row * (kMlaLat / 16), kBoxTokens * (kMlaLat / 16), bar);
-      tma_load_2d(st + kRawCodes + kRawScales + k * 2048, &tmPe, 0, (int)row, bar);
+    const uint32_t st = base + kOffRaw;
+    const uint32_t pe = base + kOffPe + (x & 1) * kPeBytes;
+    const uint32_t bar = smem_u32(&sm.raw_full), pbar = smem_u32(&sm.pe_full[x & 1]);
+    mbar_arrive_expect_tx(bar, nb * kBoxTokens * (kMlaLat / 2 + kMlaLat / 16));
+    mbar_arrive_expect_tx(pbar, nb * kBoxTokens * kMlaRope * 2);
+    for (int sub = 0; sub < 2; ++sub) {
+      const int nbs = min(4, nb - 4 * sub);
+      if (nbs <= 0) break;
+      const int tok0 = cstart + x * kT + 64 * sub;
+      const long row0 = cache_row(tok0);
+      const uint32_t o = 8192 * sub;   // 64 rows of 128 bytes
+      if (nbs == 4 && tok0 / a.ps == (tok0 + 63) / a.ps) {
+        tma_load_3d(st + o, &tmCodes64, 0, 0, (int)row0, bar);
+        tma_load_3d(st + kHalfBytes + o, &tmCodes64, 0, 1, (int)row0, bar);
+        bulk_load(st + kRawCodes + 64 * sub * (kMlaLat / 16), a.k_bscale + row0 * (kMlaLat / 16),
+                  64 * (kMlaLat / 16), bar);
+        tma_load_2d(pe + o, &tmPe64, 0, (int)row0, pbar);
+        continue;
+      }
+      for (int k = 0; k < nbs; ++k) {
+        const long row = k == 0 ? row0 : cache_row(tok0 + k * kBoxTokens);
+        tma_load_3d(st + o + k * 2048, &tmCodes, 0, 0, (int)row, bar);
+        tma_load_3d(st + kHalfBytes + o + k * 2048, &tmCodes, 0, 1, (int)row, bar);
+        bulk_load(st + kRawCodes + (64 * sub + k * kBoxTokens) * (kMlaLat / 16),
+                  a.k_bscale + row * (kMlaLat / 16), kBoxTokens * (kMlaLat / 16), bar);
+        tma_load_2d(pe + o + k * 2048, &tmPe, 0, (int)row, pbar);
+      }
     }
   };
 
-  // ================================================== S^T issue (one thread)
   if (warp == kSWarp) {
+    // ============================================== S^T issue (one thread)
     if (lane == 0) {
       const uint64_t dpe0 = sdesc(base + kOffPe, 16, 1024);
       const uint64_t dpe1 = sdesc(base + kOffPe + kPeBytes, 16, 1024);
-      // S^T MMA x: tile x decoded.  Its S^T buffer was read by the softmax of
-      // x - 2, which precedes O^T x - 2, which precedes the decode of x.
-      auto issue_s = [&](int x) {
-        const uint64_t da = (x & 1) ? dk1 : dk0;
-        const uint64_t dpe = (x & 1) ? dpe1 : dpe0;
+      int s_issued = 0;
+      for (int x = 0; x < nt && !*abort_flag; ++x) {
+        // S^T buffer x % 2 was read by the softmax of x - 2, which precedes
+        // O^T x - 2 and so the decode of x - 1 and x
         const uint32_t dl = tmem + kColSLat + 16 * (x & 1), dp = tmem + kColSPe + 16 * (x & 1);
+        for (int blk = 0; blk < kBlocks; ++blk) {
+          wait_bar(smem_u32(&sm.dec_blk[blk]), x & 1, abort_flag);
+          if (*abort_flag) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kMlaLat / 16; ++kk)
-          mma(dl, da + (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4),
-              dq + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), kIdF16, kk > 0);
+          for (int k8 = 0; k8 < 8; ++k8) {
+            const int kk = 8 * blk + k8;   // 16-dim K-step: column kk / 4 of the tile
+            mma(dl, dk + (uint64_t)(((kk >> 2) * kColBytes + (kk & 3) * 32) >> 4),
+                dq + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), kIdF16, kk > 0);
+          }
+        }
+        if (*abort_flag) break;
+        wait_bar(smem_u32(&sm.pe_full[x & 1]), (x >> 1) & 1, abort_flag);
+        if (*abort_flag) break;
+        tc_fence_after();
+        const uint64_t dpe = (x & 1) ? dpe1 : dpe0;
 #pragma unroll
         for (int kk = 0; kk < kMlaRope / 16; ++kk)
           mma(dp, dpe + (uint64_t)(kk * 2), dqpe + (uint64_t)(kk * 2), kIdBf16, kk > 0);
         mma_commit(smem_u32(&sm.s_done[x & 1]));
-      };
-      int s_issued = 0;
-      for (int x = 0; x < nt; ++x) {
-        wait_bar(smem_u32(&sm.dec_ready[x & 1]), (x >> 1) & 1, abort_flag);
-        if (*abort_flag) break;
-        tc_fence_after();
-        issue_s(x);
         ++s_issued;
       }
       // every MMA of this thread has completed at exit (bounded waits)
@@ -375,119 +395,98 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kOWarp) {
     // ============================================== O^T issue (one thread)
     if (lane == 0) {
-      const uint64_t dv0 = sdesc(base + kOffTile, 8192, 1024);   // MN-major tile
-      const uint64_t dv1 = sdesc(base + kOffTile + kTileBytes, 8192, 1024);
+      const uint64_t dv = sdesc(base + kOffTile, kColBytes, 1024);   // MN-major tile
       const uint64_t dpt0 = sdesc(base + kOffP, 16, 1024);
       const uint64_t dpt1 = sdesc(base + kOffP + kPBytes, 16, 1024);
-      // O^T MMA x: P^T x written and O rescaled (which implies S^T x done)
-      auto issue_o = [&](int x) {
-        const uint64_t da = (x & 1) ? dv1 : dv0;
-        const uint64_t dpt = (x & 1) ? dpt1 : dpt0;
-#pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-#pragma unroll
-          for (int i = 0; i < kMlaLat / 128; ++i)
-            mma(tmem + kColO + 16 * i, da + (uint64_t)(((2 * i) * 8192 + (2 * kk) * 1024) >> 4),
-                dpt + (uint64_t)(kk * 2), kIdF16MnA, x > 0 || kk > 0);
-        mma_commit(smem_u32(&sm.o_done[x & 1]));
-      };
       int o_issued = 0;
       for (int x = 0; x < nt; ++x) {
+        // P^T x written and O rescaled (which implies S^T x done)
         wait_bar(smem_u32(&sm.p_ready[x & 1]), (x >> 1) & 1, abort_flag);
         if (*abort_flag) break;
         tc_fence_after();
-        issue_o(x);
+        const uint64_t dpt = (x & 1) ? dpt1 : dpt0;
+        for (int i = 0; i < kBlocks; ++i) {
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma(tmem + kColO + 16 * i,
+                dv + (uint64_t)(((2 * i) * kColBytes + (2 * kk) * 1024) >> 4),
+                dpt + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), kIdF16MnA,
+                x > 0 || kk > 0);
+          mma_commit(smem_u32(&sm.o_blk[i]));   // block i of the tile free for x + 1
+        }
         ++o_issued;
       }
       bool ok = true;
-      for (int x = max(0, o_issued - 2); x < o_issued; ++x)
-        ok &= mbar_wait(smem_u32(&sm.o_done[x & 1]), (x >> 1) & 1);
+      if (o_issued > 0)
+        ok = mbar_wait(smem_u32(&sm.o_blk[kBlocks - 1]), (o_issued - 1) & 1);
       if (!ok || o_issued < nt) *abort_flag = 1;
     }
     __syncwarp();
-  } else {
-    // ============================================================ workers
-    // Q (decode warps): latent part as f16 (K-major [16 heads][512], 64-dim
-    // atom columns 2 KB apart), rope part as bf16 ([16][64])
-    const int dt = tid - 64;   // decode thread 0..kDecoders-1
-    // lane 0 of the last decode warp issues the copies: tiles 0 and 1 first
-    // (before the Q loads), tile y + 2 when every decode thread is done with y
+  } else if (decoder) {
+    // ============================================================ decode
+    // lane 0 of the last decode warp issues the copies: tile 0 first (before
+    // the Q conversion), tile y + 1 when every decode thread is done with y
     const bool tma_thread = warp == kWorkers / 32 - 1 && lane == 0;
-    int issued = 0;
-    if (tma_thread)
-      for (; issued < min(nt, kRawStages); ++issued) issue_raw(issued);
-    if (warp >= 2) {
-      // all of a thread's loads first: after an L2 flush each is a DRAM trip
-      constexpr int kQItems = kMlaHeads * (kMlaQkDim / 8);
-      constexpr int kQPer = (kQItems + kDecoders - 1) / kDecoders;
-      const uint16_t* qg = static_cast<const uint16_t*>(a.q) + (size_t)b * kMlaHeads * kMlaQkDim;
-      uint4 qv[kQPer];
+    if (tma_thread && nt > 0) issue_raw(0);
+    // The latent part of each head is scaled by its power of two 2^e
+    // (q_prescale_exp of the head's largest |q_lat|) before the f16
+    // conversion, so that the bf16 query keeps its full range; 2^-e goes
+    // into the head's score scale.  The rope part stays bf16 (exact).
 #pragma unroll
-      for (int k = 0; k < kQPer; ++k) {
-        const int i = dt + k * kDecoders;
-        if (i < kQItems)
-          qv[k] = *reinterpret_cast<const uint4*>(qg + (size_t)(i / (kMlaQkDim / 8)) * kMlaQkDim +
-                                                  (i % (kMlaQkDim / 8)) * 8);
-      }
-      // The latent part of each head is scaled by its power of two 2^e
-      // (q_prescale_exp of the head's largest |q_lat|) before the f16
-      // conversion, so that the bf16 query keeps its full range; 2^-e goes
-      // into the head's score scale.  The rope part stays bf16 (exact).
-#pragma unroll
-      for (int k = 0; k < kQPer; ++k) {
-        const int i = dt + k * kDecoders;
-        if (i >= kQItems) break;
-        const int h = i / (kMlaQkDim / 8), d = (i % (kMlaQkDim / 8)) * 8;
-        if (d < kMlaLat) {
-          const uint4 v = qv[k];
-          const uint32_t m2 = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                                       __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-          const uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
-          if (mx) atomicMax(&sm.qmax[h], mx);
-        }
-      }
-      asm volatile("bar.sync 3, %0;" ::"n"(kDecoders) : "memory");   // decode warps only
-#pragma unroll
-      for (int k = 0; k < kQPer; ++k) {
-        const int i = dt + k * kDecoders;
-        if (i >= kQItems) break;
-        const int h = i / (kMlaQkDim / 8), d = (i % (kMlaQkDim / 8)) * 8;
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = dt + k * kDecoders;
+      if (i >= kQItems) break;
+      const int h = i / (kMlaQkDim / 8), d = (i % (kMlaQkDim / 8)) * 8;
+      if (d < kMlaLat) {
         const uint4 v = qv[k];
-        if (d < kMlaLat) {
-          const float fs = exp2i(q_prescale_exp(sm.qmax[h]));
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-          uint32_t f[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            f[j] = pack_f16x2(__uint_as_float(w[j] << 16) * fs,
-                              __uint_as_float(w[j] & 0xFFFF0000u) * fs);
-          sts128(base + kOffQLat + (d >> 6) * 2048 + swz(h, d & 63), f[0], f[1], f[2], f[3]);
-        } else {
-          sts128(base + kOffQPe + swz(h, d - kMlaLat), v.x, v.y, v.z, v.w);
-        }
+        const uint32_t m2 = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                     __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+        const uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
+        if (mx) atomicMax(&sm.qmax[h], mx);
       }
-      if (dt < kMlaHeads) sm.qfac[dt] = scale_pow2(a.qk_scale_log2, -q_prescale_exp(sm.qmax[dt]));
-      // the softmax warps read the score scales after this barrier
-      asm volatile("bar.arrive 2, %0;" ::"n"(kDecoders + 64) : "memory");
     }
-    // Decode of tile x into tile buffer x % 2 (decode warps).  A unit is
-    // (token, 64-dim column, half) = 32 dims; eight consecutive threads take
-    // the eight tokens of an atom, so that the swizzled loads and stores
-    // spread over all banks.  Rows past the chunk are zero (finite operands
-    // for the masked tokens of the O^T MMA).  The rope keys move unchanged
-    // (same swizzled layout in the stage and in the operand tile).
-    auto decode = [&](int x) {
-      const uint32_t st = base + kOffRaw + (x % kRawStages) * kRawStage;
-      const uint32_t tile = base + kOffTile + (x & 1) * kTileBytes;
+    asm volatile("bar.sync 3, %0;" ::"n"(kDecoders) : "memory");   // decode warps only
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = dt + k * kDecoders;
+      if (i >= kQItems) break;
+      const int h = i / (kMlaQkDim / 8), d = (i % (kMlaQkDim / 8)) * 8;
+      const uint4 v = qv[k];
+      if (d < kMlaLat) {
+        const float fs = exp2i(q_prescale_exp(sm.qmax[h]));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t f[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          f[j] = pack_f16x2(__uint_as_float(w[j] << 16) * fs,
+                            __uint_as_float(w[j] & 0xFFFF0000u) * fs);
+        sts128(base + kOffQLat + (d >> 6) * 2048 + swz(h, d & 63), f[0], f[1], f[2], f[3]);
+      } else {
+        sts128(base + kOffQPe + swz(h, d - kMlaLat), v.x, v.y, v.z, v.w);
+      }
+    }
+    if (dt < kMlaHeads) sm.qfac[dt] = scale_pow2(a.qk_scale_log2, -q_prescale_exp(sm.qmax[dt]));
+    fence_proxy_async_shared();   // Q: generic stores -> operand of the async MMAs
+    // the softmax warps read the score scales after this barrier; the first
+    // S^T MMAs read Q after the first block barrier
+    asm volatile("bar.arrive 2, %0;" ::"n"(kDecoders + 32 * kSoftWarps) : "memory");
+
+    // Decode of 128-dim block blk of tile x.  A unit is (token, 64-dim
+    // column, half) = 32 dims; eight consecutive threads take the eight
+    // tokens of an atom, so that the swizzled loads and stores spread over
+    // all banks.  Rows past the chunk are zero (finite operands for the
+    // masked tokens of the O^T MMA).
+    auto decode_block = [&](int x, int blk) {
+      const uint32_t st = base + kOffRaw;
       const int nvalid = min(kT, ntok - x * kT);
-#pragma unroll 2
-      for (int u = dt; u < kT * 16; u += kDecoders) {
+#pragma unroll 1
+      for (int u = dt; u < kT * 4; u += kDecoders) {
         const int p = u & 7, rest = u >> 3;
-        const int rg = rest >> 4, db = (rest & 15) >> 1, half = rest & 1;
+        const int rg = rest >> 2, db = 2 * blk + ((rest >> 1) & 1), half = rest & 1;
         const int r = rg * 8 + p;
         uint32_t o[4][4];
         if (r < nvalid) {
-          const uint4 v = lds128(st + (db >> 2) * (kRawCodes / 2) + r * 128 +
+          const uint4 v = lds128(st + (db >> 2) * kHalfBytes + r * 128 +
                                  (((((db & 3) * 2 + half) ^ r) & 7) << 4));
           const uint32_t sc = lds16(st + kRawCodes + r * (kMlaLat / 16) + db * 4 + half * 2);
           const uint32_t s2 = e4m3x2_to_f16x2(sc);
@@ -507,159 +506,129 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0u;
         }
-        const uint32_t row_base = tile + db * 8192 + (r >> 3) * 1024 + (r & 7) * 128;
+        const uint32_t row_base =
+            base + kOffTile + db * kColBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           sts128(row_base + ((((half * 4 + k) ^ r) & 7) << 4), o[k][0], o[k][1], o[k][2],
                  o[k][3]);
       }
-      const uint32_t pe_src = st + kRawCodes + kRawScales;
-      const uint32_t pe_dst = base + kOffPe + (x & 1) * kPeBytes;
-#pragma unroll 1
-      for (int i = dt; i < kPeBytes / 16; i += kDecoders) {
-        const uint4 v = lds128(pe_src + i * 16);
-        sts128(pe_dst + i * 16, v.x, v.y, v.z, v.w);
-      }
       fence_proxy_async_shared();   // generic stores -> operands of the async MMAs
-      mbar_arrive(smem_u32(&sm.dec_ready[x & 1]));
+      mbar_arrive(smem_u32(&sm.dec_blk[blk]));
     };
 
-    // O rescale of the 32 tensor-memory lanes of this warp's sub-partition
-    // (the reference max of some heads moved at tile t; O^T MMA t-1 done)
-    auto rescale_o = [&](int t) {
-      wait_bar(smem_u32(&sm.o_done[(t - 1) & 1]), ((t - 1) >> 1) & 1, abort_flag);
-      tc_fence_after();
-      const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-#pragma unroll 1
-      for (int i = 0; i < kMlaLat / 128; ++i) {
-        uint32_t v[16];
-        tmem_ld16(lane_addr + kColO + 16 * i, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int h = 0; h < kMlaHeads; ++h)
-          v[h] = __float_as_uint(__uint_as_float(v[h]) * sm.alpha[t & 1][h]);
-        tmem_st16(lane_addr + kColO + 16 * i, v);
+    int issued = nt > 0 ? 1 : 0;
+    for (int x = 0; x < nt && !*abort_flag; ++x) {
+      wait_bar(smem_u32(&sm.raw_full), x & 1, abort_flag);
+      for (int blk = 0; blk < kBlocks && !*abort_flag; ++blk) {
+        // block blk of the tile buffer was last read by O^T x - 1 (and S^T
+        // x - 1, which completed before it)
+        if (x > 0) wait_bar(smem_u32(&sm.o_blk[blk]), (x - 1) & 1, abort_flag);
+        decode_block(x, blk);
       }
-      tmem_wait_st();
-      tc_fence_before();
-    };
-
-    if (warp >= 2) {
-      // ---- decode warps: tile t+1 (its buffer was last read by O^T MMA
-      // t-1); warps 2-3 also take lanes 64..127 of an O rescale of tile t
-      auto refill = [&](int y) {
-        if (tma_thread && issued < nt) {
-          wait_bar(smem_u32(&sm.dec_ready[y & 1]), (y >> 1) & 1, abort_flag);
-          if (!*abort_flag) issue_raw(issued++);
-        }
-      };
-      if (nt > 0) {
-        wait_bar(smem_u32(&sm.raw_full[0]), 0, abort_flag);
-        decode(0);
-        refill(0);
+      // the raw buffer is free once every decode thread is done with tile x
+      if (tma_thread && issued < nt) {
+        wait_bar(smem_u32(&sm.dec_blk[kBlocks - 1]), x & 1, abort_flag);
+        if (!*abort_flag) issue_raw(issued++);
       }
-      int nresc = 0;
-      for (int t = 0; t < nt && !*abort_flag; ++t) {
-        if (t + 1 < nt) {
-          if (t >= 1) wait_bar(smem_u32(&sm.o_done[(t - 1) & 1]), ((t - 1) >> 1) & 1, abort_flag);
-          wait_bar(smem_u32(&sm.raw_full[(t + 1) % kRawStages]), ((t + 1) / kRawStages) & 1,
-                   abort_flag);
-          decode(t + 1);
-          refill(t + 1);
-        }
-        if (warp < 4) {
-          wait_bar(smem_u32(&sm.p_done[t & 1]), (t >> 1) & 1, abort_flag);
-          if (sm.rescale[t & 1] && !*abort_flag) {
-            rescale_o(t);
-            mbar_arrive(smem_u32(&sm.resc_done));
-            ++nresc;
-          }
-        }
-      }
-      if (tma_thread) {
-        if (!dep_done) griddep_wait();   // the grid ends after the append it overlapped
-        // no copy in flight at exit (bounded waits)
-        for (int x = max(0, issued - kRawStages); x < issued; ++x)
-          mbar_wait(smem_u32(&sm.raw_full[x % kRawStages]), (x / kRawStages) & 1);
-      }
-    } else {
-      // ---- softmax warps: tile t, one token per thread, all 16 heads
-      asm volatile("bar.sync 2, %0;" ::"n"(kDecoders + 64) : "memory");   // score scales written
-      float qf[kMlaHeads];
-#pragma unroll
-      for (int h = 0; h < kMlaHeads; ++h) qf[h] = sm.qfac[h];
-      int nresc = 0;
-      for (int t = 0; t < nt; ++t) {
-        wait_bar(smem_u32(&sm.s_done[t & 1]), (t >> 1) & 1, abort_flag);
-        tc_fence_after();
-        uint32_t sl[16], sp[16];
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
-        tmem_ld16(lane_addr + kColSLat + 16 * (t & 1), sl);
-        tmem_ld16(lane_addr + kColSPe + 16 * (t & 1), sp);
-        tmem_wait_ld();
-        const int r = 32 * warp + lane;
-        const bool valid = r < ntok - t * kT && !*abort_flag;
-        float xs[kMlaHeads];
-        bool need = false;
-#pragma unroll
-        for (int h = 0; h < kMlaHeads; ++h) {
-          xs[h] = valid ? __uint_as_float(sl[h]) * qf[h] +
-                              __uint_as_float(sp[h]) * a.pe_scale_log2
-                        : -INFINITY;
-          need |= xs[h] > m[h] + kLazyMax;
-        }
-        need = __any_sync(0xffffffffu, need);
-        if (lane == 0) sm.need[warp] = need;
-        asm volatile("bar.sync 1, 64;" ::: "memory");
-        const bool any_need = sm.need[0] | sm.need[1];
-        bool resc = false;
-        if (any_need) {
-#pragma unroll
-          for (int h = 0; h < kMlaHeads; ++h) {
-            float mx = xs[h];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            if (lane == 0) sm.wmax[warp][h] = mx;
-          }
-          asm volatile("bar.sync 1, 64;" ::: "memory");
-#pragma unroll
-          for (int h = 0; h < kMlaHeads; ++h) {
-            const float mx = fmaxf(sm.wmax[0][h], sm.wmax[1][h]);
-            const bool mv = mx > m[h] + kLazyMax;   // also the first finite tile
-            const float alpha = mv ? ex2(m[h] - mx) : 1.f;
-            m[h] = mv ? mx : m[h];
-            l[h] *= alpha;
-            resc |= alpha != 1.f;
-            if (tid == 0) sm.alpha[t & 1][h] = alpha;
-          }
-        }
-        const bool do_resc = any_need && resc && t > 0;   // identical in all 64 threads
-        if (tid == 0) sm.rescale[t & 1] = do_resc ? 1 : 0;
-        const uint32_t pt = base + kOffP + (t & 1) * kPBytes;
-#pragma unroll
-        for (int h = 0; h < kMlaHeads; ++h) {
-          const float pv = ex2(xs[h] - (m[h] == -INFINITY ? 0.f : m[h]));
-          l[h] += pv;
-          sts16(pt + swz(h, r), __half_as_ushort(__float2half_rn(pv)));
-        }
-        fence_proxy_async_shared();
-        tc_fence_before();
-        asm volatile("bar.sync 1, 64;" ::: "memory");   // both warps' P^T and flags written
-        if (tid == 0) mbar_arrive(smem_u32(&sm.p_done[t & 1]));
-        if (do_resc) {
-          rescale_o(t);
-          asm volatile("bar.sync 1, 64;" ::: "memory");
-          if (tid == 0) wait_bar(smem_u32(&sm.resc_done), nresc & 1, abort_flag);
-          ++nresc;
-        }
-        if (tid == 0) mbar_arrive(smem_u32(&sm.p_ready[t & 1]));   // O^T MMA t may go
-        asm volatile("bar.sync 1, 64;" ::: "memory");
-        if (*abort_flag) break;
+    }
+    if (tma_thread) {
+      if (!dep_done) griddep_wait();   // the grid ends after the append it overlapped
+      // no copy in flight at exit (bounded waits)
+      if (issued > 0) {
+        mbar_wait(smem_u32(&sm.raw_full), (issued - 1) & 1);
+        mbar_wait(smem_u32(&sm.pe_full[(issued - 1) & 1]), ((issued - 1) >> 1) & 1);
       }
     }
   }
-  // denominators over the 64 tokens of the softmax warps; the reference max
-  if (warp < 2) {
+
+  // softmax state (warps 0-3: one token per thread, all 16 heads)
+  float m[kMlaHeads], l[kMlaHeads];
+#pragma unroll
+  for (int h = 0; h < kMlaHeads; ++h) m[h] = -INFINITY, l[h] = 0.f;
+  if (warp < kSoftWarps) {
+    // ============================================================ softmax
+    asm volatile("bar.sync 2, %0;" ::"n"(kDecoders + 32 * kSoftWarps) : "memory");
+    float qf[kMlaHeads];
+#pragma unroll
+    for (int h = 0; h < kMlaHeads; ++h) qf[h] = sm.qfac[h];
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+    for (int t = 0; t < nt; ++t) {
+      wait_bar(smem_u32(&sm.s_done[t & 1]), (t >> 1) & 1, abort_flag);
+      tc_fence_after();
+      uint32_t sl[16], sp[16];
+      tmem_ld16(lane_addr + kColSLat + 16 * (t & 1), sl);
+      tmem_ld16(lane_addr + kColSPe + 16 * (t & 1), sp);
+      tmem_wait_ld();
+      const int r = tid;   // token of the tile
+      const bool valid = r < ntok - t * kT && !*abort_flag;
+      float xs[kMlaHeads];
+      bool need = false;
+#pragma unroll
+      for (int h = 0; h < kMlaHeads; ++h) {
+        xs[h] = valid ? __uint_as_float(sl[h]) * qf[h] + __uint_as_float(sp[h]) * a.pe_scale_log2
+                      : -INFINITY;
+        need |= xs[h] > m[h] + kLazyMax;
+      }
+      need = __any_sync(0xffffffffu, need);
+      if (lane == 0) sm.need[warp] = need;
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftWarps) : "memory");
+      const bool any_need = sm.need[0] | sm.need[1] | sm.need[2] | sm.need[3];
+      bool resc = false;
+      float alpha[kMlaHeads];
+      if (any_need) {
+#pragma unroll
+        for (int h = 0; h < kMlaHeads; ++h) {
+          float mx = xs[h];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          if (lane == 0) sm.wmax[warp][h] = mx;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftWarps) : "memory");
+#pragma unroll
+        for (int h = 0; h < kMlaHeads; ++h) {
+          const float mx = fmaxf(fmaxf(sm.wmax[0][h], sm.wmax[1][h]),
+                                 fmaxf(sm.wmax[2][h], sm.wmax[3][h]));
+          const bool mv = mx > m[h] + kLazyMax;   // also the first finite tile
+          alpha[h] = mv ? ex2(m[h] - mx) : 1.f;
+          m[h] = mv ? mx : m[h];
+          l[h] *= alpha[h];
+          resc |= alpha[h] != 1.f;
+        }
+      }
+      // identical in all softmax threads: the maxima come from shared memory
+      const bool do_resc = any_need && resc && t > 0;
+      const uint32_t pt = base + kOffP + (t & 1) * kPBytes + (r >> 6) * 2048;
+#pragma unroll
+      for (int h = 0; h < kMlaHeads; ++h) {
+        const float pv = ex2(xs[h] - (m[h] == -INFINITY ? 0.f : m[h]));
+        l[h] += pv;
+        sts16(pt + swz(h, r & 63), __half_as_ushort(__float2half_rn(pv)));
+      }
+      if (do_resc) {
+        // O of the tensor-memory lanes of this warp (value dims 128 i +
+        // 32 w + lane), once O^T t - 1 has completed
+        wait_bar(smem_u32(&sm.o_blk[kBlocks - 1]), (t - 1) & 1, abort_flag);
+        tc_fence_after();
+#pragma unroll 1
+        for (int i = 0; i < kBlocks; ++i) {
+          uint32_t v[16];
+          tmem_ld16(lane_addr + kColO + 16 * i, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < kMlaHeads; ++h)
+            v[h] = __float_as_uint(__uint_as_float(v[h]) * alpha[h]);
+          tmem_st16(lane_addr + kColO + 16 * i, v);
+        }
+        tmem_wait_st();
+      }
+      fence_proxy_async_shared();
+      tc_fence_before();
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftWarps) : "memory");   // all of P^T and O
+      if (tid == 0) mbar_arrive(smem_u32(&sm.p_ready[t & 1]));   // O^T MMAs t may go
+      if (*abort_flag) break;
+    }
+    // denominators over the tile's tokens; the reference max
 #pragma unroll
     for (int h = 0; h < kMlaHeads; ++h) {
       float v = l[h];
@@ -677,16 +646,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- partials: warp w < 4 holds dims 128 i + 32 w + lane of every block i
   const size_t part_row = (size_t)b * kMlaHeads;
-  if (warp < 4) {
+  if (warp < kSoftWarps) {
     float fac[kMlaHeads];
 #pragma unroll
     for (int h = 0; h < kMlaHeads; ++h) {
-      const float lt = sm.lsum[0][h] + sm.lsum[1][h];
+      const float lt = (sm.lsum[0][h] + sm.lsum[1][h]) + (sm.lsum[2][h] + sm.lsum[3][h]);
       fac[h] = lt > 0.f ? __fdividef(a.out_mult, lt) : 0.f;
     }
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll 1
-    for (int i = 0; i < kMlaLat / 128; ++i) {
+    for (int i = 0; i < kBlocks; ++i) {
       uint32_t v[16];
       if (nt > 0 && !bad) {
         tmem_ld16(lane_addr + kColO + 16 * i, v);
@@ -702,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (tid < kMlaHeads) {
-    const float lt = sm.lsum[0][tid] + sm.lsum[1][tid];
+    const float lt = (sm.lsum[0][tid] + sm.lsum[1][tid]) + (sm.lsum[2][tid] + sm.lsum[3][tid]);
     const float mm = sm.m[tid];
     a.part_lse[(part_row + tid) * a.num_splits + split] =
         bad ? NAN : (mm == -INFINITY || lt == 0.f) ? -INFINITY : (mm + log2f(lt)) * kLn2;
@@ -717,10 +686,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                  : "memory");
   }
   // fused combine: the partials of the request (16 x s x 512 floats) staged
-  // in the two tile buffers (128 KB), the weights in the raw ring
+  // in the tile buffer (128 KB), the weights in the raw buffer
   if (a.counters)
     fused_combine_staged<32, 4>(a, b, part_row, kMlaHeads, base + kOffTile,
-                                reinterpret_cast<const float*>(gbase + kOffTile), 2 * kTileBytes,
+                                reinterpret_cast<const float*>(gbase + kOffTile), kTileBytes,
                                 reinterpret_cast<float*>(gbase + kOffRaw), smem_u32(&sm.comb_full));
 }
 }  // namespace
