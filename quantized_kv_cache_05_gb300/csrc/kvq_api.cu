@@ -290,9 +290,10 @@ kvq_status kvq_auto_splits(int num_sms, int batch, int num_kv_heads, int q_per_k
                            int max_kv_len, int fmt, int* out_s) {
   if (!out_s || num_sms < 1 || batch < 1 || num_kv_heads < 1 || max_kv_len < 0)
     return KVQ_ERR_INVALID;
-  // One wave of the partial kernel (three resident CTAs per SM, two with
-  // more than eight query heads per kv head, one for the MLA kernel: NVFP4,
-  // one kv head, 16 query heads), and chunks of at most kTargetChunk tokens,
+  // One wave of the partial kernel (two resident six-warp CTAs per SM, or
+  // three four-warp CTAs without wide CTAs; two with more than eight query
+  // heads per kv head; one for the MLA kernel: NVFP4, one kv head, 16 query
+  // heads), and chunks of at most kTargetChunk tokens,
   // so that long or ragged requests are cut into pieces that balance across
   // the waves.
   // More than kManySplits splits of chunks shorter than kShortChunk tokens
@@ -302,7 +303,7 @@ kvq_status kvq_auto_splits(int num_sms, int batch, int num_kv_heads, int q_per_k
   constexpr long long kMinChunk = 128, kMaxSplits = 64, kTargetChunk = 2048;
   constexpr long long kShortChunk = 256, kManySplits = 32;
   const bool mla_shape = fmt == KVQ_NVFP4 && num_kv_heads == 1 && q_per_kv == 16;
-  const long long ctas_per_sm = mla_shape ? 1 : q_per_kv > 8 ? 2 : 3;
+  const long long ctas_per_sm = mla_shape ? 1 : q_per_kv > 8 ? 2 : kWideCta ? 2 : 3;
   const long long base = (long long)batch * num_kv_heads;
   long long s = ctas_per_sm * num_sms / base;
   s = std::max(s, ((long long)max_kv_len + kTargetChunk - 1) / kTargetChunk);

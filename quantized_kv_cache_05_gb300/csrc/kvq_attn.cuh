@@ -24,7 +24,6 @@ struct Geom {
   // unswizzled 32-byte rows)
   static constexpr int kAlign = kRow >= 64 ? 1024 : 128;
   static constexpr int kStage = (2 * (kBoxK + kBoxS) + kAlign - 1) / kAlign * kAlign;
-  static constexpr int kRing = kDecodeWarps * kStages * kStage;
   // FP8-probability mode streams K and V in separate sweeps: a stage holds
   // one box of one tensor, [codes][scales]
   static constexpr int kStage1 = (kBoxK + kBoxS + kAlign - 1) / kAlign * kAlign;

@@ -9,12 +9,16 @@
 // s partials.  FP8 probabilities and FP8 output follow vLLM PR 15734.
 //
 // GB300 design of the partial kernel
-//  * Four warps per CTA, three CTAs per SM (four in the FP8-probability
-//    mode, whose ring holds one tensor per stage).  Each warp streams its own
-//    16-token boxes (box w, w+4, w+8, ... of the chunk) HBM -> shared memory
-//    with TMA (cp.async.bulk.tensor, 16-row box = one 16-token page,
-//    hardware swizzle; NVFP4 block scales by 1-D bulk copies) into a private
-//    4-deep ring with its own mbarriers, and consumes them itself: no
+//  * NW warps per CTA: six, two CTAs per SM, for the common decode (up to 8
+//    query heads per kv head, head_dim <= 128, no FP8 probabilities); four
+//    otherwise (three CTAs per SM, four in the FP8-probability mode, whose
+//    ring holds one tensor per stage).  Twelve warps per SM either way; the
+//    six-warp CTAs leave a third fewer split partials for the merge.  Each
+//    warp streams its own 16-token boxes (box w, w+NW, w+2NW, ... of the
+//    chunk) HBM -> shared memory with TMA (cp.async.bulk.tensor, 16-row box
+//    = one 16-token page, hardware swizzle; NVFP4 block scales by 1-D bulk
+//    copies) into a private 3-deep ring with its own mbarriers, and consumes
+//    them itself: no
 //    producer warp, no cross-warp hand-off per box, and twelve warps per SM
 //    issuing copies (one issuing thread per CTA cannot keep HBM busy).  The
 //    chunk's block-table entries are cached in shared memory.
@@ -55,25 +59,26 @@
 namespace kvq {
 namespace decode_impl {
 
+template <int NW>
 struct Smem {
-  uint64_t full[kDecodeWarps][kStages];
+  uint64_t full[NW][kStages];
   uint64_t comb_full;   // fused combine: partials landed
   int abort_flag;
   int pages[kPageCache];
-  float m[kDecodeWarps][kMaxGroup];
-  float l[kDecodeWarps][kMaxGroup];
-  float fac[kDecodeWarps][kMaxGroup];
+  float m[NW][kMaxGroup];
+  float l[NW][kMaxGroup];
+  float fac[NW][kMaxGroup];
 };
 
 // Shared-memory ring of the partial kernel: the TMA stages, reused after the
 // loop for the warps' O fragments and the fused combine's weights.
-template <int FMT, int D, bool PROBQ, int NH>
+template <int FMT, int D, bool PROBQ, int NH, int NW>
 struct Ring {
   using Gm = Geom<FMT, D>;
   static constexpr int kStageBytes = PROBQ ? Gm::kStage1 : Gm::kStage;
-  static constexpr int kEpilogue = kDecodeWarps * Gm::kMT * NH * 32 * 16 +
+  static constexpr int kEpilogue = NW * Gm::kMT * NH * 32 * 16 +
                                    (kMaxGroup * kMaxFusedSplits + kMaxGroup) * 4;
-  static constexpr int kStream = kDecodeWarps * kStages * kStageBytes;
+  static constexpr int kStream = NW * kStages * kStageBytes;
   static constexpr int kBytes =
       kStream > kEpilogue ? kStream : (kEpilogue + 1023) / 1024 * 1024;
 };
@@ -82,8 +87,10 @@ struct Ring {
 // ring of the FP8-probability mode with up to eight query heads per kv head,
 // three otherwise, two with sixteen heads (twice the accumulators); head_dim
 // 256 has twice the fragments and ring of 128: two, one with sixteen heads.
-template <int FMT, int D, bool PROBQ, int NH>
+// Six-warp CTAs (NW = 6): two per SM.
+template <int FMT, int D, bool PROBQ, int NH, int NW>
 constexpr int ctas_per_sm() {
+  if (NW == 6) return 2;
   if (D >= 256) return NH == 2 ? 1 : 2;
   return NH == 2 ? 2 : PROBQ ? 4 : 3;
 }
@@ -91,8 +98,8 @@ constexpr int ctas_per_sm() {
 // NH = number of 8-head groups (1: up to 8 query heads per kv head, 2: up to
 // 16); QF8: the query is E4M3 codes (FP8 query), and with an FP8 cache the
 // scores run on the E4M3 x E4M3 MMA straight from the cached code bytes.
-template <int FMT, int D, bool PROBQ, int NH, bool QF8>
-__global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>())
+template <int FMT, int D, bool PROBQ, int NH, bool QF8, int NW>
+__global__ void __launch_bounds__(32 * NW, ctas_per_sm<FMT, D, PROBQ, NH, NW>())
     partial_kernel(const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PartialArgs a) {
   using Gm = Geom<FMT, D>;
@@ -103,7 +110,7 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
   constexpr int kSweeps = PROBQ ? 2 : 1;
 
   extern __shared__ uint8_t dyn_smem[];
-  __shared__ Smem sm;
+  __shared__ Smem<NW> sm;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -113,7 +120,7 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
 
   // ring base, aligned for the 128-byte swizzle pattern
   const uint32_t ring = (smem_u32(dyn_smem) + 1023u) & ~1023u;
-  using Rg = Ring<FMT, D, PROBQ, NH>;
+  using Rg = Ring<FMT, D, PROBQ, NH, NW>;
   const uint32_t scores = ring + Rg::kBytes;   // FP8-prob mode only
 
   const int cap = min(a.max_pages * a.ps, a.max_kv_len);
@@ -148,15 +155,15 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
   // first box of the chunk that holds an appended position (overlap mode)
   const int fresh_box = a.fresh == 0 ? 0 : (max(L - a.fresh, cstart) - cstart) / kBoxTokens;
   bool dep_done = a.fresh == 0;   // this thread has waited for the preceding kernel
-  // this warp's boxes: warp, warp + 4, ...
-  const int nw = nboxes > warp ? (nboxes - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
+  // this warp's boxes: warp, warp + NW, ...
+  const int nw = nboxes > warp ? (nboxes - warp + NW - 1) / NW : 0;
   const int total = kSweeps * nw;
 
   // block-table entries of the chunk -> shared memory
   const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
   const int p0 = cstart / a.ps;
   const int npages = cend > cstart ? (cend - 1) / a.ps - p0 + 1 : 0;
-  for (int i = threadIdx.x; i < min(npages, kPageCache); i += kDecodeThreads) {
+  for (int i = threadIdx.x; i < min(npages, kPageCache); i += (32 * NW)) {
     int pg = __ldg(bt + p0 + i);
     if (pg < 0 || pg >= a.num_pages) {
       record_error(a.error_flag, 4);
@@ -168,15 +175,15 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
   volatile int* abort_flag = &sm.abort_flag;
 
   // Issue the copies of this warp's j-th load (lane 0 only) into stage st:
-  // load j covers box w + 4 (j % nw); in FP8-prob mode loads [0, nw) bring
+  // load j covers box w + NW (j % nw); in FP8-prob mode loads [0, nw) bring
   // K, [nw, 2nw) V.  Loads are issued in order; the page and in-page offset
-  // of the next one advance by 64 tokens per load (no division per box).
+  // of the next one advance by 16 NW tokens per load (no division per box).
   const int tok_first = cstart + warp * kBoxTokens;
   int nx_pidx = tok_first / a.ps;
   int nx_off = tok_first - nx_pidx * a.ps;
   auto issue = [&](int j, int st) {
     const int sweep = PROBQ ? (j >= nw ? 1 : 0) : 0;
-    const int box = warp + kDecodeWarps * (j - sweep * nw);
+    const int box = warp + NW * (j - sweep * nw);
     const bool loadK = !PROBQ || sweep == 0;
     const bool loadV = !PROBQ || sweep == 1;
     if (PROBQ && j == nw) {   // the V sweep starts over at the warp's first box
@@ -184,7 +191,7 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
       nx_off = tok_first - nx_pidx * a.ps;
     }
     const int pidx = nx_pidx, off = nx_off;
-    nx_off += kDecodeWarps * kBoxTokens;
+    nx_off += NW * kBoxTokens;
     while (nx_off >= a.ps) {
       nx_off -= a.ps;
       ++nx_pidx;
@@ -330,7 +337,7 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
         break;
       }
       __syncwarp();   // the other lanes read the box after lane 0's acquire
-      const int tbase = cstart + (warp + kDecodeWarps * jj) * kBoxTokens;
+      const int tbase = cstart + (warp + NW * jj) * kBoxTokens;
       const int nvalid = min(kBoxTokens, cend - tbase);
       const uint32_t sbase = ring + (warp * kStages + st) * Rg::kStageBytes;
       const uint32_t boxK = sbase;
@@ -526,7 +533,7 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
           for (int e = 0; e < 2; ++e) {
             float mm = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kDecodeWarps; ++w) mm = fmaxf(mm, sm.m[w][2 * t + e + 8 * hh]);
+            for (int w = 0; w < NW; ++w) mm = fmaxf(mm, sm.m[w][2 * t + e + 8 * hh]);
             m[hh][e] = mm;
           }
         __syncthreads();
@@ -585,11 +592,11 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
   if (threadIdx.x < a.G) {
     const int row = threadIdx.x;
     float M = -INFINITY;
-    for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, sm.m[w][row]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, sm.m[w][row]);
     float Ltot = 0.f;
-    for (int w = 0; w < kDecodeWarps; ++w)
+    for (int w = 0; w < NW; ++w)
       if (sm.m[w][row] != -INFINITY) Ltot += ex2(sm.m[w][row] - M) * sm.l[w][row];
-    for (int w = 0; w < kDecodeWarps; ++w)
+    for (int w = 0; w < NW; ++w)
       sm.fac[w][row] = (M == -INFINITY || sm.m[w][row] == -INFINITY || Ltot == 0.f)
                            ? 0.f
                            : ex2(sm.m[w][row] - M) / Ltot * out_mult;
@@ -601,13 +608,13 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
 
   // ---------------------------------------------------------------- merge
   // item (i, hh, lane'): heads h0 = 2t' + 8hh and h0 + 1, dims d0 and d0 + 1
-  for (int it = threadIdx.x; it < MT * NH * 32; it += kDecodeThreads) {
+  for (int it = threadIdx.x; it < MT * NH * 32; it += (32 * NW)) {
     const int ln = it & 31, hh = (it >> 5) % NH, i = (it >> 5) / NH;
     const int h0 = 2 * (ln & 3) + 8 * hh;
     if (h0 >= a.G) continue;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < kDecodeWarps; ++w) {
+    for (int w = 0; w < NW; ++w) {
       const float4 v = ofrag[((w * MT + i) * NH + hh) * 32 + ln];
       const float f0 = sm.fac[w][h0], f1 = sm.fac[w][h0 + 1];
       acc.x += f0 * v.x;
@@ -632,16 +639,16 @@ __global__ void __launch_bounds__(kDecodeThreads, ctas_per_sm<FMT, D, PROBQ, NH>
     uint32_t dyn_bytes;
     asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
     const uint32_t usable = dyn_bytes - (ring - smem_u32(dyn_smem));
-    fused_combine_staged<ctas_per_sm<FMT, D, PROBQ, NH>() == 4 ? 16 : 32>(
+    fused_combine_staged<ctas_per_sm<FMT, D, PROBQ, NH, NW>() == 4 ? 16 : 32>(
         a, bh, part_row, a.G, ring, reinterpret_cast<const float*>(ofrag), usable - kWbuf,
         reinterpret_cast<float*>(dyn_smem + (ring - smem_u32(dyn_smem)) + usable - kWbuf),
         smem_u32(&sm.comb_full));
   }
 }
 
-template <int FMT, int D, bool PROBQ, int NH, bool QF8>
+template <int FMT, int D, bool PROBQ, int NH, bool QF8, int NW>
 cudaError_t launch_partial_t(const TensorMaps& m, const PartialArgs& a, cudaStream_t st) {
-  using Rg = Ring<FMT, D, PROBQ, NH>;
+  using Rg = Ring<FMT, D, PROBQ, NH, NW>;
   static_assert(Rg::kBytes >= Rg::kEpilogue && Rg::kBytes >= Rg::kStream, "ring too small");
   size_t smem = 1024 + (size_t)Rg::kBytes + (PROBQ ? (size_t)a.score_floats * 4 : 0);
   if (a.counters) {
@@ -649,30 +656,33 @@ cudaError_t launch_partial_t(const TensorMaps& m, const PartialArgs& a, cudaStre
     // floats, and the weights) in one bulk copy, within the shared memory
     // that keeps ctas_per_sm CTAs resident (228 KB per SM, 1 KB reserved per
     // CTA, the static part under 4 KB, the alignment slack)
-    constexpr size_t kPerCta = 233472 / ctas_per_sm<FMT, D, PROBQ, NH>() - 1024 - 4096 - 1024;
+    constexpr size_t kPerCta = 233472 / ctas_per_sm<FMT, D, PROBQ, NH, NW>() - 1024 - 4096 - 1024;
     const size_t need = 1024 + (size_t)a.G * a.num_splits * a.Dv * 4 +
                         (kMaxGroup * kMaxFusedSplits + kMaxGroup) * 4;
     smem = std::max(smem, std::min(need, kPerCta));
   }
   smem = (smem + 15) / 16 * 16;
-  auto kern = partial_kernel<FMT, D, PROBQ, NH, QF8>;
+  auto kern = partial_kernel<FMT, D, PROBQ, NH, QF8, NW>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(a.batch * a.Hkv, a.num_splits), dim3(kDecodeThreads), smem, st,
+  return launch_pdl(kern, dim3(a.batch * a.Hkv, a.num_splits), dim3(32 * NW), smem, st,
                     m.k16, m.v16, a);
 }
 
 template <int FMT, int D, bool QF8>
 cudaError_t dispatch_nh(bool probq, const TensorMaps& m, const PartialArgs& a, cudaStream_t st) {
-  if (a.G <= 8)
-    return probq ? launch_partial_t<FMT, D, true, 1, QF8>(m, a, st)
-                 : launch_partial_t<FMT, D, false, 1, QF8>(m, a, st);
-  return probq ? launch_partial_t<FMT, D, true, 2, QF8>(m, a, st)
-               : launch_partial_t<FMT, D, false, 2, QF8>(m, a, st);
+  if (a.G <= 8) {
+    if (probq) return launch_partial_t<FMT, D, true, 1, QF8, kDecodeWarps>(m, a, st);
+    if constexpr (D <= 128)
+      if (wide_cta(D, false, a.G)) return launch_partial_t<FMT, D, false, 1, QF8, kWideWarps>(m, a, st);
+    return launch_partial_t<FMT, D, false, 1, QF8, kDecodeWarps>(m, a, st);
+  }
+  return probq ? launch_partial_t<FMT, D, true, 2, QF8, kDecodeWarps>(m, a, st)
+               : launch_partial_t<FMT, D, false, 2, QF8, kDecodeWarps>(m, a, st);
 }
 
 template <int FMT, int D>

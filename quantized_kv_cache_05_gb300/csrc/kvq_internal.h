@@ -17,6 +17,14 @@ constexpr int kFmtNvfp4 = 2;
 constexpr int kBoxTokens = 16;    // tokens per TMA box (one 16-token page) = one MMA k-tile
 constexpr int kDecodeWarps = 4;   // each warp streams and consumes its own boxes
 constexpr int kDecodeThreads = 32 * kDecodeWarps;
+// Wide CTAs: six decode warps, two CTAs per SM, for the common decode (no
+// FP8 probabilities, up to 8 query heads per kv head, head_dim <= 128): the
+// same twelve warps per SM as three four-warp CTAs, but a third fewer split
+// partials, so that the fused merge of long sequences stages them in shared
+// memory with one copy.
+constexpr bool kWideCta = true;
+constexpr int kWideWarps = 6;
+inline bool wide_cta(int D, bool probq, int G) { return kWideCta && !probq && G <= 8 && D <= 128; }
 constexpr int kStages = 3;        // boxes in flight per warp (3 measured equal or faster than 4)
 constexpr int kMaxGroup = 16;     // query heads per kv head (two 8-head MMA tiles)
 constexpr int kScoreCapacity = 16384;  // fp32 scores per CTA in FP8-prob mode

@@ -63,18 +63,19 @@ def test_tensor_scale_matches_oracle(orc):
 
 def test_auto_splits():
     f = kvq.kvq_auto_splits
-    # 152 SMs, GQA 2 x 8 kv heads: floor(3 * 152 / 16) = 28 (one wave of 448 CTAs)
-    assert f(152, 2, 8, 4, 32768, 1) == (0, 28)
-    assert f(152, 2, 8, 4, 8192, 1) == (0, 28)
+    # 152 SMs, GQA 2 x 8 kv heads, two six-warp CTAs per SM: floor(2 * 152 / 16) = 19
+    # (one wave of 304 CTAs)
+    assert f(152, 2, 8, 4, 32768, 1) == (0, 19)
+    assert f(152, 2, 8, 4, 8192, 1) == (0, 19)
     # short sequences: at least 128 tokens per chunk
     assert f(152, 2, 8, 4, 1024, 1) == (0, 8)
     assert f(152, 2, 8, 4, 100, 1) == (0, 1)
-    # batch 1 x 8 kv heads: floor(456 / 8) = 57
-    assert f(152, 1, 8, 4, 32768, 2) == (0, 57)
-    assert f(152, 1, 8, 4, 16384, 2) == (0, 57)
+    # batch 1 x 8 kv heads: floor(304 / 8) = 38
+    assert f(152, 1, 8, 4, 32768, 2) == (0, 38)
+    assert f(152, 1, 8, 4, 16384, 2) == (0, 38)
+    assert f(152, 1, 8, 4, 12288, 2) == (0, 38)
     # more than 32 splits of chunks under 256 tokens: max(32, ceil(L / 256))
-    assert f(152, 1, 8, 4, 14336, 2) == (0, 56)
-    assert f(152, 1, 8, 4, 12288, 2) == (0, 48)
+    assert f(152, 1, 8, 4, 9216, 2) == (0, 36)
     assert f(152, 1, 8, 4, 8192, 2) == (0, 32)
     assert f(152, 1, 8, 4, 8192, 1) == (0, 32)
     assert f(152, 1, 8, 4, 2048, 2) == (0, 16)
