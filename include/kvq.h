@@ -97,7 +97,7 @@ typedef struct kvq_cache {
   int32_t num_pages;         /* >= 1 */
   int32_t page_size;         /* tokens per page, a multiple of 16 */
   int32_t num_kv_heads;      /* Hkv >= 1 */
-  int32_t head_dim;          /* D: FP8 64 or 128; NVFP4 128 (MLA 512) */
+  int32_t head_dim;          /* D: FP8 64 or 128; NVFP4 64, 128 or 256 (MLA 512) */
   void* k_codes;             /* (device) 16-byte aligned */
   void* v_codes;             /* (device) 16-byte aligned; NULL for MLA */
   void* k_bscale;            /* (device) NVFP4 only, 16-byte aligned */
@@ -218,8 +218,9 @@ kvq_status kvq_quantize_append(const kvq_cache* c, const void* k_new, const void
 /*
  * Split-count heuristic (host only, deterministic).  base = batch *
  * num_kv_heads (MLA: batch) CTAs per split; the partial kernel keeps
- * ctas_per_sm CTAs resident per SM (3; 2 when q_per_kv > 8; 1 for the MLA
- * shape: KVQ_NVFP4, num_kv_heads 1, q_per_kv 16), so
+ * ctas_per_sm CTAs resident per SM (2: six-warp CTAs, or four-warp CTAs
+ * with more than 8 query heads per kv head; 1 for the MLA shape:
+ * KVQ_NVFP4, num_kv_heads 1, q_per_kv 16), so
  * floor(ctas_per_sm * num_sms / base) splits fill one wave;
  * s is at least ceil(max_kv_len / 2048), so that long or ragged requests
  * are cut into chunks that balance across waves.  Above 32 splits with
