@@ -17,10 +17,10 @@
 //    warp streams its own 16-token boxes (box w, w+NW, w+2NW, ... of the
 //    chunk) HBM -> shared memory with TMA (cp.async.bulk.tensor, 16-row box
 //    = one 16-token page, hardware swizzle; NVFP4 block scales by 1-D bulk
-//    copies) into a private 3-deep ring with its own mbarriers, and consumes
-//    them itself: no
-//    producer warp, no cross-warp hand-off per box, and twelve warps per SM
-//    issuing copies (one issuing thread per CTA cannot keep HBM busy).  The
+//    copies) into a private 2-deep (six warps) or 3-deep ring with its own
+//    mbarriers, and consumes them itself: no producer warp, no cross-warp
+//    hand-off per box, and twelve warps per SM issuing copies (one issuing
+//    thread per CTA cannot keep HBM busy).  The
 //    chunk's block-table entries are cached in shared memory.
 //  * Codes are decoded in registers straight into tensor-core fragments
 //    (E4M3 -> f16 and E2M1 -> f16 with cvt, block scales by an f16x2
@@ -59,9 +59,16 @@
 namespace kvq {
 namespace decode_impl {
 
+// Boxes in flight per warp: two for six-warp CTAs, three for four-warp ones
+// (measured: with six-warp CTAs two stages gave the shorter GQA steps, 34.9
+// against 35.3 us at 32k and 20.3 against 20.8 at 8k; four were slower in
+// every mode).
+template <int NW>
+constexpr int ring_stages() { return NW == kWideWarps ? 2 : kStages; }
+
 template <int NW>
 struct Smem {
-  uint64_t full[NW][kStages];
+  uint64_t full[NW][ring_stages<NW>()];
   uint64_t comb_full;   // fused combine: partials landed
   int abort_flag;
   int pages[kPageCache];
@@ -78,7 +85,7 @@ struct Ring {
   static constexpr int kStageBytes = PROBQ ? Gm::kStage1 : Gm::kStage;
   static constexpr int kEpilogue = NW * Gm::kMT * NH * 32 * 16 +
                                    (kMaxGroup * kMaxFusedSplits + kMaxGroup) * 4;
-  static constexpr int kStream = NW * kStages * kStageBytes;
+  static constexpr int kStream = NW * ring_stages<NW>() * kStageBytes;
   static constexpr int kBytes =
       kStream > kEpilogue ? kStream : (kEpilogue + 1023) / 1024 * 1024;
 };
@@ -103,6 +110,7 @@ __global__ void __launch_bounds__(32 * NW, ctas_per_sm<FMT, D, PROBQ, NH, NW>())
     partial_kernel(const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PartialArgs a) {
   using Gm = Geom<FMT, D>;
+  constexpr int kRingStages = ring_stages<NW>();
   constexpr int KS = Gm::kKSteps;
   constexpr bool kRawK = QF8 && FMT == kFmtFp8;   // scores on e4m3 x e4m3 (k32)
   constexpr int KS8 = D / 32;                      // its k-steps
@@ -131,7 +139,7 @@ __global__ void __launch_bounds__(32 * NW, ctas_per_sm<FMT, D, PROBQ, NH, NW>())
   // positions: then only the loads of boxes holding those positions wait.
   if (threadIdx.x == 0) sm.abort_flag = 0;
   if (lane == 0) {
-    for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&sm.full[warp][i]), 1);
+    for (int i = 0; i < kRingStages; ++i) mbar_init(smem_u32(&sm.full[warp][i]), 1);
     if (warp == 0) mbar_init(smem_u32(&sm.comb_full), 1);
     fence_barrier_init();
   }
@@ -212,7 +220,7 @@ __global__ void __launch_bounds__(32 * NW, ctas_per_sm<FMT, D, PROBQ, NH, NW>())
       dep_done = true;
     }
     const uint32_t full = smem_u32(&sm.full[warp][st]);
-    const uint32_t sbase = ring + (warp * kStages + st) * Rg::kStageBytes;
+    const uint32_t sbase = ring + (warp * kRingStages + st) * Rg::kStageBytes;
     const uint32_t bytes = (loadK ? Gm::kBoxK + Gm::kBoxS : 0) + (loadV ? Gm::kBoxK + Gm::kBoxS : 0);
     mbar_arrive_expect_tx(full, bytes);
     if constexpr (PROBQ) {   // one tensor per stage: [codes][scales]
@@ -234,7 +242,7 @@ __global__ void __launch_bounds__(32 * NW, ctas_per_sm<FMT, D, PROBQ, NH, NW>())
   int issued = 0;
   if (lane == 0) {
 #pragma unroll 1   // one copy of the issue code (it runs cold, once per CTA)
-    for (; issued < min(total, kStages); ++issued) issue(issued, issued);
+    for (; issued < min(total, kRingStages); ++issued) issue(issued, issued);
   }
 
   const int hq0 = h * a.G;
@@ -339,7 +347,7 @@ __global__ void __launch_bounds__(32 * NW, ctas_per_sm<FMT, D, PROBQ, NH, NW>())
       __syncwarp();   // the other lanes read the box after lane 0's acquire
       const int tbase = cstart + (warp + NW * jj) * kBoxTokens;
       const int nvalid = min(kBoxTokens, cend - tbase);
-      const uint32_t sbase = ring + (warp * kStages + st) * Rg::kStageBytes;
+      const uint32_t sbase = ring + (warp * kRingStages + st) * Rg::kStageBytes;
       const uint32_t boxK = sbase;
       const uint32_t boxV = PROBQ ? sbase : sbase + Gm::kBoxK;
       const uint32_t boxKs = PROBQ ? sbase + Gm::kBoxK : sbase + 2 * Gm::kBoxK;
@@ -504,13 +512,13 @@ __global__ void __launch_bounds__(32 * NW, ctas_per_sm<FMT, D, PROBQ, NH, NW>())
             mma_f16(o[i][hh], va[i][0], va[i][1], va[i][2], va[i][3], pl[hh][0], pl[hh][1]);
           }
       }
-      // the box is consumed: refill its stage with this warp's load j + kStages
+      // the box is consumed: refill its stage with this warp's load j + kRingStages
       __syncwarp();
       if (lane == 0 && issued < total) {
         fence_proxy_async_shared();   // generic reads of the stage before the async overwrite
         issue(issued++, st);
       }
-      if (++st == kStages) {
+      if (++st == kRingStages) {
         st = 0;
         phase ^= 1u;
       }
@@ -547,8 +555,8 @@ __global__ void __launch_bounds__(32 * NW, ctas_per_sm<FMT, D, PROBQ, NH, NW>())
   // Drain: no copy of this warp may still be writing shared memory later.
   if (lane == 0) {
     const int done = aborted ? 0 : total;
-    for (int k = max(done, issued - kStages); k < issued; ++k)
-      mbar_wait(smem_u32(&sm.full[warp][k % kStages]), (k / kStages) & 1);
+    for (int k = max(done, issued - kRingStages); k < issued; ++k)
+      mbar_wait(smem_u32(&sm.full[warp][k % kRingStages]), (k / kRingStages) & 1);
   }
   __syncwarp();
   // per-warp state -> shared memory (m is uniform over the 8 lanes of a

@@ -25,7 +25,7 @@ constexpr int kDecodeThreads = 32 * kDecodeWarps;
 constexpr bool kWideCta = true;
 constexpr int kWideWarps = 6;
 inline bool wide_cta(int D, bool probq, int G) { return kWideCta && !probq && G <= 8 && D <= 128; }
-constexpr int kStages = 3;        // boxes in flight per warp (3 measured equal or faster than 4)
+constexpr int kStages = 3;        // boxes in flight per warp of a four-warp CTA (3 measured equal or faster than 4)
 constexpr int kMaxGroup = 16;     // query heads per kv head (two 8-head MMA tiles)
 constexpr int kScoreCapacity = 16384;  // fp32 scores per CTA in FP8-prob mode
 constexpr int kPageCache = 512;   // block-table entries of a chunk kept in shared memory
