@@ -16,8 +16,9 @@
 //  * TMA copies bring a tile's latent codes (128-byte swizzled boxes) and
 //    block scales (1-D bulk copies) into a raw buffer, and its rope keys
 //    straight into one of two bf16 operand tiles (the same swizzled layout);
-//    lane 0 of the last decode warp issues them once the previous tile has
-//    been decoded;
+//    the O^T issuing thread issues those of the first tile (it is idle
+//    until the first P^T), lane 0 of the last decode warp those of every
+//    later tile once the previous tile has been decoded;
 //  * six decode warps turn the tile, once, into an f16 [token][dim] tile
 //    (E2M1 x E4M3 -> f16 is exact) in the 128-byte-swizzled layout that is
 //    the K-major A operand of S^T = K Q^T and, read MN-major, the A operand
@@ -313,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t dqpe = sdesc(base + kOffQPe, 16, 1024);
   const uint64_t dk = sdesc(base + kOffTile, 16, 1024);   // K-major tile
 
-  // Copies of tile x (by lane 0 of the last decode warp): codes and scales
+  // Copies of tile x (tile 0 by the O^T thread, later ones by lane 0 of the
+  // last decode warp): codes and scales
   // into the raw buffer, rope keys into rope tile x % 2.  Each 64-token half
   // inside one page moves as four copies (64-row boxes), otherwise as four
   // per 16-token box.  Raw layout: codes [half][row][128 B] (128-byte
@@ -395,6 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kOWarp) {
     // ============================================== O^T issue (one thread)
     if (lane == 0) {
+      // the copies of tile 0: this thread is idle until its first P^T, and
+      // the decode warps convert Q meanwhile
+      if (nt > 0) issue_raw(0);
       const uint64_t dv = sdesc(base + kOffTile, kColBytes, 1024);   // MN-major tile
       const uint64_t dpt0 = sdesc(base + kOffP, 16, 1024);
       const uint64_t dpt1 = sdesc(base + kOffP + kPBytes, 16, 1024);
@@ -424,10 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (decoder) {
     // ============================================================ decode
-    // lane 0 of the last decode warp issues the copies: tile 0 first (before
-    // the Q conversion), tile y + 1 when every decode thread is done with y
+    // lane 0 of the last decode warp issues the copies of tile y + 1 when
+    // every decode thread is done with tile y (tile 0: the O^T thread)
     const bool tma_thread = warp == kWorkers / 32 - 1 && lane == 0;
-    if (tma_thread && nt > 0) issue_raw(0);
     // The latent part of each head is scaled by its power of two 2^e
     // (q_prescale_exp of the head's largest |q_lat|) before the f16
     // conversion, so that the bf16 query keeps its full range; 2^-e goes
