@@ -149,6 +149,12 @@ __global__ void __launch_bounds__(32 * NW, ctas_per_sm<FMT, D, PROBQ, NH, NW>())
   }
   if (a.fresh == 0) griddep_wait();
 
+  // one-page requests: the page index does not depend on the length, so its
+  // load overlaps the length's
+  const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
+  int pg_single = 0;
+  if (a.max_pages == 1 && threadIdx.x == 0) pg_single = __ldg(bt);
+
   // chunk of this split
   int L = a.seq_lens[b];
   if (L > cap || L < 0) {
@@ -168,11 +174,10 @@ __global__ void __launch_bounds__(32 * NW, ctas_per_sm<FMT, D, PROBQ, NH, NW>())
   const int total = kSweeps * nw;
 
   // block-table entries of the chunk -> shared memory
-  const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
   const int p0 = cstart / a.ps;
   const int npages = cend > cstart ? (cend - 1) / a.ps - p0 + 1 : 0;
   for (int i = threadIdx.x; i < min(npages, kPageCache); i += (32 * NW)) {
-    int pg = __ldg(bt + p0 + i);
+    int pg = a.max_pages == 1 ? pg_single : __ldg(bt + p0 + i);
     if (pg < 0 || pg >= a.num_pages) {
       record_error(a.error_flag, 4);
       pg = 0;

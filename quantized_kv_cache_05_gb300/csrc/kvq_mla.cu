@@ -259,6 +259,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // one-page requests: the page index does not depend on the length, so its
+  // load overlaps the length's
+  const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
+  int pg_single = 0;
+  if (a.max_pages == 1 && tid == 0) pg_single = __ldg(bt);
+
   // ---- chunk of this split
   int L = a.seq_lens[b];
   const int cap = min(a.max_pages * a.ps, a.max_kv_len);
@@ -275,11 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int fresh_tok = a.fresh == 0 ? 0x7fffffff : max(L - a.fresh, cstart) - cstart;
   bool dep_done = a.fresh == 0;   // issuer: has waited for the preceding kernel
 
-  const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
   const int p0 = cstart / a.ps;
   const int npages = cend > cstart ? (cend - 1) / a.ps - p0 + 1 : 0;
   for (int i = tid; i < min(npages, kPageCache); i += kThreads) {
-    int pg = __ldg(bt + p0 + i);
+    int pg = a.max_pages == 1 ? pg_single : __ldg(bt + p0 + i);
     if (pg < 0 || pg >= a.num_pages) {
       record_error(a.error_flag, 4);
       pg = 0;
