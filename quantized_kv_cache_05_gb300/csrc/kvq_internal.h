@@ -15,8 +15,7 @@ constexpr int kFmtNvfp4 = 2;
 
 // Decode pipeline geometry shared by host and device code.
 constexpr int kBoxTokens = 16;    // tokens per TMA box (one 16-token page) = one MMA k-tile
-constexpr int kDecodeWarps = 4;   // each warp streams and consumes its own boxes
-constexpr int kDecodeThreads = 32 * kDecodeWarps;
+constexpr int kDecodeWarps = 4;   // warps of a four-warp CTA; each streams and consumes its own boxes
 // Wide CTAs: six decode warps, two CTAs per SM, for the common decode (no
 // FP8 probabilities, up to 8 query heads per kv head, head_dim <= 128): the
 // same twelve warps per SM as three four-warp CTAs, but a third fewer split
