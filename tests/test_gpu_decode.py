@@ -361,3 +361,24 @@ def test_mla_partials_per_chunk(mla):
                     continue
                 assert abs(pl[b, hq, j] - l) <= 1e-4 * max(1.0, abs(l)), (b, hq, j)
                 assert_f32_close(po[b, hq, j], o, f"mla partial b{b} h{hq} j{j}")
+
+
+@pytest.mark.parametrize("fmt,hq,hkv,d", [("fp8", 8, 8, 128), ("fp8", 16, 2, 64), ("nvfp4", 8, 8, 64),
+                                          ("nvfp4", 8, 1, 128), ("fp8", 6, 2, 128)])
+def test_six_warp_ctas(fmt, hq, hkv, d):
+    """The six-warp CTAs (up to 8 query heads per kv head, head_dim <= 128):
+    MHA, 8:1 and 3:1 groups, head_dim 64 and 128, ragged lengths whose box
+    counts are not multiples of six warps (and shorter than six boxes), in the
+    two-launch and the fused path."""
+    w = synth.gqa_fp8(1500) if fmt == "fp8" else synth.nvfp4(1500)
+    w.B, w.Hq, w.Hkv, w.D = 3, hq, hkv, d
+    w.seq_lens = np.array([1500, 83, 997], np.int32)
+    S = Setup(w)
+    ref, _ = S.oracle_decode()
+    for s in (1, 5, 0):
+        s = splits_of(w, s)
+        out, _ = S.gpu_decode(s)
+        assert_f32_close(out.cpu().numpy(), ref, f"{fmt} {hq}:{hkv} D={d} s={s}")
+        b, ws = fused(S, s)
+        assert_f32_close(b.cpu().numpy(), ref, f"fused {fmt} {hq}:{hkv} D={d} s={s}")
+        assert not ws.counters.any()
