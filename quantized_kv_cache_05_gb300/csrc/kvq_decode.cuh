@@ -244,10 +244,17 @@ __global__ void __launch_bounds__(32 * NW, ctas_per_sm<FMT, D, PROBQ, NH, NW>())
     }
   };
 
+  // FP8 caches, short chunks (fewer than 8 loads per warp): only the first
+  // load of every warp goes out now, the rest of the ring once the query is
+  // loaded, so the grid's first burst of copies is smaller and every warp's
+  // first box lands sooner (GQA FP8 8k: step 19.7 -> 18.9 us).  Long chunks,
+  // and NVFP4 (whose decode work per box is the bottleneck: 8k 0.5 us
+  // slower deferred), fill the ring at once.
+  const int early = (FMT == kFmtFp8 && total < 8) ? 1 : kRingStages;
   int issued = 0;
   if (lane == 0) {
 #pragma unroll 1   // one copy of the issue code (it runs cold, once per CTA)
-    for (; issued < min(total, kRingStages); ++issued) issue(issued, issued);
+    for (; issued < min(total, early); ++issued) issue(issued, issued);
   }
 
   const int hq0 = h * a.G;
@@ -322,6 +329,11 @@ __global__ void __launch_bounds__(32 * NW, ctas_per_sm<FMT, D, PROBQ, NH, NW>())
       qsc[hh][0] = __shfl_sync(0xffffffffu, my, 4 * (2 * t));
       qsc[hh][1] = __shfl_sync(0xffffffffu, my, 4 * (2 * t + 1));
     }
+  }
+
+  if (lane == 0) {
+#pragma unroll 1
+    for (; issued < min(total, kRingStages); ++issued) issue(issued, issued);
   }
 
   // O^T accumulators: m-tile i (value dims), head group hh; C layout
