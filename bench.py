@@ -654,7 +654,11 @@ def sweep(device, args):
              ("paged_fp8_probs", lambda L: synth.paged_fp8_probs(), [0], [1, 2, 0]),
              ("mla_nvfp4", lambda L: synth.mla_nvfp4(), [0], [1, 2, 4, 8, 0]),
              ("gqa_fp8_head_scales", synth.gqa_fp8_head_scales, [8192, 32768], [0]),
-             ("gqa_fp8_query", synth.gqa_fp8_query, [8192, 32768], [0])]
+             ("gqa_fp8_query", synth.gqa_fp8_query, [8192, 32768], [0]),
+             # larger batches of the GQA FP8 shape: bandwidth sustained once the
+             # step's bytes dwarf its fixed latency (not one of the five configs)
+             ("gqa_fp8_B16", lambda L: synth.gqa_fp8_batch(16, L), [8192], [0]),
+             ("gqa_fp8_B8", lambda L: synth.gqa_fp8_batch(8, L), [32768], [0])]
     for name, mk, lens, splits in plans:
         for L in lens:
             w = mk(L) if L else mk(None)

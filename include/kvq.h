@@ -221,9 +221,10 @@ kvq_status kvq_quantize_append(const kvq_cache* c, const void* k_new, const void
  * ctas_per_sm CTAs resident per SM (2: six-warp CTAs, or four-warp CTAs
  * with more than 8 query heads per kv head; 1 for the MLA shape:
  * KVQ_NVFP4, num_kv_heads 1, q_per_kv 16), so
- * floor(ctas_per_sm * num_sms / base) splits fill one wave;
- * s is at least ceil(max_kv_len / 2048), so that long or ragged requests
- * are cut into chunks that balance across waves.  Above 32 splits with
+ * s = floor(ctas_per_sm * num_sms / base) splits fill one wave; when that
+ * is 0 (more groups than one wave holds), s = ceil(max_kv_len / 2048), so
+ * that long or ragged requests are cut into chunks that balance across the
+ * waves.  Above 32 splits with
  * chunks under 256 tokens (max_kv_len < 256 s), s becomes
  * max(32, ceil(max_kv_len / 256)).  s is then lowered so that every chunk
  * keeps at least 128 tokens and clamped to [1, 64].  num_sms is

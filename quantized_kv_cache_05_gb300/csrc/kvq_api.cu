@@ -290,12 +290,16 @@ kvq_status kvq_auto_splits(int num_sms, int batch, int num_kv_heads, int q_per_k
                            int max_kv_len, int fmt, int* out_s) {
   if (!out_s || num_sms < 1 || batch < 1 || num_kv_heads < 1 || max_kv_len < 0)
     return KVQ_ERR_INVALID;
-  // One wave of the partial kernel (two resident six-warp CTAs per SM, or
-  // three four-warp CTAs without wide CTAs; two with more than eight query
-  // heads per kv head; one for the MLA kernel: NVFP4, one kv head, 16 query
-  // heads), and chunks of at most kTargetChunk tokens,
-  // so that long or ragged requests are cut into pieces that balance across
-  // the waves.
+  // When the (request, kv head) groups fit in one wave of the partial kernel
+  // (two resident six-warp CTAs per SM, or three four-warp CTAs without wide
+  // CTAs; two with more than eight query heads per kv head; one for the MLA
+  // kernel: NVFP4, one kv head, 16 query heads), s fills that wave: a partly
+  // filled second wave costs more than idle slots in the first (GQA FP8 batch
+  // 16 x 8 kv heads at 8192 tokens: 52.3 us at s = 2, one wave, against 57.3
+  // at s = 4 and 69.3 at s = 3; batch 8 at 32768: 91.6 us at s = 4 against
+  // 106.6 at s = 16 and 128.7 at s = 5).  When they do not, the grid runs in
+  // several waves anyway and chunks of at most kTargetChunk tokens cut long
+  // or ragged requests into pieces that balance across them.
   // More than kManySplits splits of chunks shorter than kShortChunk tokens
   // lose to fewer, longer chunks (per-CTA fixed cost; the fused merge stages
   // about 30 splits in shared memory): measured on 8 kv-head groups at 8192
@@ -306,7 +310,7 @@ kvq_status kvq_auto_splits(int num_sms, int batch, int num_kv_heads, int q_per_k
   const long long ctas_per_sm = mla_shape ? 1 : q_per_kv > 8 ? 2 : kWideCta ? 2 : 3;
   const long long base = (long long)batch * num_kv_heads;
   long long s = ctas_per_sm * num_sms / base;
-  s = std::max(s, ((long long)max_kv_len + kTargetChunk - 1) / kTargetChunk);
+  if (s < 1) s = ((long long)max_kv_len + kTargetChunk - 1) / kTargetChunk;
   if (s > kManySplits && (long long)max_kv_len < s * kShortChunk)
     s = std::max(kManySplits, ((long long)max_kv_len + kShortChunk - 1) / kShortChunk);
   const long long by_len = max_kv_len / kMinChunk;

@@ -307,6 +307,17 @@ def paged_fp8_probs(B: int = 64, lo: int = 512, hi: int = 8192, seed: int = 0) -
                     permute_pages=True, prob_fp8=True, out="e4m3", splits=(1, 0), seed=seed)
 
 
+def gqa_fp8_batch(B: int, L: int) -> Workload:
+    """The GQA FP8 shapes and values with a larger batch (B requests of L
+    tokens): a decode step with enough bytes that the launch's fixed latency
+    is a small part of it."""
+    w = gqa_fp8(L)
+    w.name = f"gqa_fp8_B{B}_L{L}"
+    w.B = B
+    w.seq_lens = np.full(B, L, np.int32)
+    return w
+
+
 def gqa_fp8_head_scales(L: int = 8192) -> Workload:
     """The GQA FP8 workload with per-kv-head static scales (compressed-tensors
     PR 436 "attn_head" strategy): same shapes and values, one scale per kv

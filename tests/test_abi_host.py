@@ -79,14 +79,19 @@ def test_auto_splits():
     assert f(152, 1, 8, 4, 8192, 2) == (0, 32)
     assert f(152, 1, 8, 4, 8192, 1) == (0, 32)
     assert f(152, 1, 8, 4, 2048, 2) == (0, 16)
-    # large batch: chunks of at most 2048 tokens (ceil(8192 / 2048) = 4)
+    # more groups than one wave holds (1024 > 304): chunks of at most 2048 tokens
+    # (ceil(8192 / 2048) = 4)
     assert f(152, 64, 16, 1, 8192, 1) == (0, 4)
     assert f(152, 64, 16, 1, 2048, 1) == (0, 1)
     assert f(152, 64, 16, 1, 2049, 1) == (0, 2)
-    assert f(152, 4, 8, 4, 200000, 1) == (0, 64)
+    # groups that fit one wave fill it, whatever the length: floor(304 / 32) = 9,
+    # floor(304 / 128) = 2, floor(304 / 64) = 4 (a partial second wave costs more)
+    assert f(152, 4, 8, 4, 200000, 1) == (0, 9)
+    assert f(152, 16, 8, 4, 8192, 1) == (0, 2)
+    assert f(152, 8, 8, 4, 32768, 1) == (0, 4)
     # MLA shape (NVFP4, 16 heads on one kv head: one CTA per SM): floor(152 / 32) = 4
     assert f(152, 32, 1, 16, 4096, 2) == (0, 4)
-    assert f(152, 128, 1, 16, 4096, 2) == (0, 2)
+    assert f(152, 128, 1, 16, 4096, 2) == (0, 1)
     # 16 FP8 heads on one kv head: two CTAs per SM, floor(304 / 32) = 9
     assert f(152, 32, 1, 16, 4096, 1) == (0, 9)
     assert f(152, 2, 1, 12, 32768, 1) == (0, 64)
