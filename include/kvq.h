@@ -271,6 +271,10 @@ kvq_status kvq_decode_combine(const kvq_decode_params* p, const float* part_o,
  * One decode step in a single launch: kvq_decode_partial followed by the
  * merge of kvq_decode_combine, which the last CTA to finish for each
  * (request, kv head) performs with the same arithmetic and output types.
+ * MLA with 2..8 splits runs as thread-block clusters of a request's splits
+ * when they fit the device in as many waves as single CTAs: the partials
+ * then merge through distributed shared memory (part_o and part_lse are not
+ * written, the counters not used), with the same results bit for bit.
  *   part_o, part_lse (device) split partials, as for kvq_decode_partial.
  *   counters (device) uint32 [batch * num_kv_heads] arrival counters.  They
  *   must be zero before the first call; every call leaves them at zero

@@ -525,4 +525,88 @@ __device__ __forceinline__ void fused_combine_staged(const PartialArgs& a, int b
   if (!ok && threadIdx.x == 0) record_error(a.error_flag, 1);
 }
 
+// Merge through distributed shared memory, for a launch in clusters of the
+// s <= 8 splits of a request (cluster rank = split): every CTA holds its
+// normalized partial [rows][Dv] fp32 at shared address `own` and its lse
+// [rows] at `own_lse`.  After a cluster barrier one thread per row forms the
+// row's weights from the peers' lse, and CTA rank r computes items
+// [r n / s, (r + 1) n / s) of the n = rows Dv / 4 (row, 4 value dims) items,
+// loading each item's s partials from the peers' shared memory in one round;
+// a second barrier keeps every CTA's shared memory until its peers are done.
+// No partial goes to global memory and no arrival counter is used.
+//
+// The result is bit for bit that of the global-memory merge: the weights are
+// merge_weights' (the max is order-free; its butterfly sum over 32 lanes, of
+// which lanes >= s hold exact zeros, is for s <= 8 the pairwise sum
+// ((e0 + e4) + (e2 + e6)) + ((e1 + e5) + (e3 + e7)) with e_j = 0 for j >= s),
+// and the weighted sum runs in split order like accum_splits.
+// wbuf: kMaxGroup * (kMaxFusedSplits + 1) floats of this CTA's shared memory.
+// (Measured on MLA: loading two items per thread before the weights, or
+// forming the weights in every thread, made the merge slower.)
+constexpr int kMaxClusterSplits = 8;   // portable cluster size
+
+template <int DT>
+__device__ __forceinline__ void merge_cluster_items(const PartialArgs& a, size_t row0, int rows,
+                                                    uint32_t own, const float* w,
+                                                    const float* winv) {
+  const int s = a.num_splits, nq = a.Dv / 4, n = rows * nq;
+  const int rank = (int)cluster_ctarank();
+  const int i0 = (int)(((long)n * rank) / s), i1 = (int)(((long)n * (rank + 1)) / s);
+  uint32_t peer[kMaxClusterSplits];
+#pragma unroll
+  for (int j = 0; j < kMaxClusterSplits; ++j) peer[j] = cluster_map(own, j < s ? j : 0);
+#pragma unroll 1
+  for (int i = i0 + (int)threadIdx.x; i < i1; i += blockDim.x) {
+    const int r = i / nq, d4 = i % nq;
+    const uint32_t off = (uint32_t)(r * a.Dv + 4 * d4) * 4u;
+    float4 v[kMaxClusterSplits];
+#pragma unroll
+    for (int j = 0; j < kMaxClusterSplits; ++j)
+      if (j < s) v[j] = ld_cluster_v4(peer[j] + off);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < kMaxClusterSplits; ++j)
+      if (j < s) {
+        const float wj = w[r * kMaxFusedSplits + j];
+        acc.x += wj * v[j].x;
+        acc.y += wj * v[j].y;
+        acc.z += wj * v[j].z;
+        acc.w += wj * v[j].w;
+      }
+    store_item<DT>(a, row0, r, d4, acc, winv[r]);
+  }
+}
+
+__device__ __forceinline__ void fused_combine_cluster(const PartialArgs& a, size_t row0, int rows,
+                                                      uint32_t own, uint32_t own_lse,
+                                                      float* wbuf) {
+  cluster_sync_all();   // every split's partial and lse are written
+  const int s = a.num_splits;
+  float* winv = wbuf + kMaxGroup * kMaxFusedSplits;
+  if ((int)threadIdx.x < rows) {
+    const int r = threadIdx.x;
+    float lv[kMaxClusterSplits];
+    float M = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMaxClusterSplits; ++j) {
+      lv[j] = j < s ? ld_cluster_f32(cluster_map(own_lse + 4u * r, j)) : -INFINITY;
+      M = fmaxf(M, lv[j]);
+    }
+    float* wr = wbuf + r * kMaxFusedSplits;
+#pragma unroll 1
+    for (int j = 0; j < kMaxClusterSplits; ++j)
+      wr[j] = (j >= s || M == -INFINITY || lv[j] == -INFINITY) ? 0.f : expf(lv[j] - M);
+    const float sum = ((wr[0] + wr[4]) + (wr[2] + wr[6])) + ((wr[1] + wr[5]) + (wr[3] + wr[7]));
+    winv[r] = sum > 0.f ? 1.f / sum : (sum == 0.f ? 0.f : NAN);
+  }
+  __syncthreads();
+  if (a.out_dtype == 0)
+    merge_cluster_items<0>(a, row0, rows, own, wbuf, winv);
+  else if (a.out_dtype == 1)
+    merge_cluster_items<1>(a, row0, rows, own, wbuf, winv);
+  else
+    merge_cluster_items<2>(a, row0, rows, own, wbuf, winv);
+  cluster_sync_all();   // the peers have read this CTA's partial
+}
+
 }  // namespace kvq

@@ -41,6 +41,8 @@
 // double buffered.  Every wait is bounded; a timeout sets an error bit and
 // the partials become NaN.
 
+#include <atomic>
+
 #include "kvq_attn.cuh"
 
 namespace kvq {
@@ -99,6 +101,7 @@ struct MlaSmem {
   float wmax[kSoftWarps][kMlaHeads];   // per-warp tile maxima
   float lsum[kSoftWarps][kMlaHeads];   // per-warp denominators (end)
   float m[kMlaHeads];              // final reference max (end)
+  float fac[kMlaHeads];            // partial's factor per head: value scale / denominator (end)
   uint32_t qmax[kMlaHeads];        // largest |q_lat| per head (bf16 magnitude bits)
   float qfac[kMlaHeads];           // latent score scale per head (log2 domain)
   int pages[kPageCache];
@@ -653,37 +656,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool bad = *abort_flag != 0;
   if (bad && tid == 0) record_error(a.error_flag, 1);
 
-  // ---- partials: warp w < 4 holds dims 128 i + 32 w + lane of every block i
+  // ---- partials: warp w < 4 holds dims 128 i + 32 w + lane of every block i;
+  // to global memory, or (cluster merge) to this CTA's shared memory:
+  // [head][512] floats in the free tile buffer, the lse after them
   const size_t part_row = (size_t)b * kMlaHeads;
-  if (warp < kSoftWarps) {
-    float fac[kMlaHeads];
-#pragma unroll
-    for (int h = 0; h < kMlaHeads; ++h) {
-      const float lt = (sm.lsum[0][h] + sm.lsum[1][h]) + (sm.lsum[2][h] + sm.lsum[3][h]);
-      fac[h] = lt > 0.f ? __fdividef(a.out_mult, lt) : 0.f;
-    }
-    const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
-#pragma unroll 1
-    for (int i = 0; i < kBlocks; ++i) {
-      uint32_t v[16];
-      if (nt > 0 && !bad) {
-        tmem_ld16(lane_addr + kColO + 16 * i, v);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int h = 0; h < kMlaHeads; ++h) v[h] = 0u;
-      }
-      float* po = a.part_o + (part_row * a.num_splits + split) * kMlaLat + 128 * i + 32 * warp + lane;
-#pragma unroll
-      for (int h = 0; h < kMlaHeads; ++h)
-        po[(size_t)h * a.num_splits * kMlaLat] = bad ? NAN : __uint_as_float(v[h]) * fac[h];
-    }
-  }
+  const bool cl = a.cluster_merge != 0;
+  float* own = reinterpret_cast<float*>(gbase + kOffTile);
+  float* own_lse = own + kMlaHeads * kMlaLat;
+  // one thread per head: the factor and the lse (this code runs cold, once
+  // per CTA: one short sequence instead of sixteen per thread)
   if (tid < kMlaHeads) {
     const float lt = (sm.lsum[0][tid] + sm.lsum[1][tid]) + (sm.lsum[2][tid] + sm.lsum[3][tid]);
+    sm.fac[tid] = bad ? NAN : lt > 0.f ? __fdividef(a.out_mult, lt) : 0.f;
     const float mm = sm.m[tid];
-    a.part_lse[(part_row + tid) * a.num_splits + split] =
+    const float lse =
         bad ? NAN : (mm == -INFINITY || lt == 0.f) ? -INFINITY : (mm + log2f(lt)) * kLn2;
+    if (cl)
+      own_lse[tid] = lse;
+    else
+      a.part_lse[(part_row + tid) * a.num_splits + split] = lse;
+  }
+  if (warp < kSoftWarps) {
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftWarps) : "memory");   // factors written
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+    // the four blocks' accumulators in one round trip
+    uint32_t v[kBlocks][16];
+    if (nt > 0 && !bad) {
+#pragma unroll
+      for (int i = 0; i < kBlocks; ++i) tmem_ld16(lane_addr + kColO + 16 * i, v[i]);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int i = 0; i < kBlocks; ++i)
+#pragma unroll
+        for (int h = 0; h < kMlaHeads; ++h) v[i][h] = 0u;
+    }
+    const size_t hstride = cl ? (size_t)kMlaLat : (size_t)a.num_splits * kMlaLat;
+    float* po = (cl ? own : a.part_o + (part_row * a.num_splits + split) * kMlaLat) + 32 * warp + lane;
+#pragma unroll
+    for (int h = 0; h < kMlaHeads; ++h) {
+      const float f = sm.fac[h];
+#pragma unroll
+      for (int i = 0; i < kBlocks; ++i) po[(size_t)h * hstride + 128 * i] = __uint_as_float(v[i][h]) * f;
+    }
   }
   // ---- tensor memory back; then the fused combine
   tc_fence_before();
@@ -694,23 +709,80 @@ __global__ void __launch_bounds__(kThreads, 1)
                  "r"(kTmemCols)
                  : "memory");
   }
-  // fused combine: the partials of the request (16 x s x 512 floats) staged
-  // in the tile buffer (128 KB), the weights in the raw buffer
-  if (a.counters)
+  // fused combine: through the cluster's shared memory, or with the
+  // partials of the request (16 x s x 512 floats) staged in the tile buffer
+  // (128 KB) and the weights in the raw buffer
+  if (cl)
+    fused_combine_cluster(a, part_row, kMlaHeads, base + kOffTile,
+                          base + kOffTile + kMlaHeads * kMlaLat * 4,
+                          reinterpret_cast<float*>(gbase + kOffRaw));
+  else if (a.counters)
     fused_combine_staged<32, 4>(a, b, part_row, kMlaHeads, base + kOffTile,
                                 reinterpret_cast<const float*>(gbase + kOffTile), kTileBytes,
                                 reinterpret_cast<float*>(gbase + kOffRaw), smem_u32(&sm.comb_full));
 }
 }  // namespace
 
+namespace {
+// Clusters of s CTAs of this kernel that fit on the device at once (cached
+// per device and s; 0 when the query fails).
+int mla_max_clusters(int dev, int s) {
+  constexpr int kDevs = 64;
+  static std::atomic<int> cache[kDevs][kMaxClusterSplits + 1];
+  if (dev < 0 || dev >= kDevs) return 0;
+  const int c = cache[dev][s].load(std::memory_order_relaxed);
+  if (c > 0) return c - 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(1, s);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)s;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, mla_tc_kernel, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  cache[dev][s].store(n + 1, std::memory_order_relaxed);
+  return n;
+}
+}  // namespace
+
+// The fused decode (arrival counters given) with 2..8 splits runs as
+// clusters of the s splits of a request, whose partials then merge through
+// distributed shared memory, when the clusters that fit at once cover the
+// grid in no more waves than single CTAs would (one CTA per SM).
 cudaError_t launch_mla_partial(const CUtensorMap& tcodes, const CUtensorMap& tpe,
                                const CUtensorMap& tcodes64, const CUtensorMap& tpe64,
                                const PartialArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(mla_tc_kernel, dim3(a.batch, a.num_splits), dim3(kThreads),
-                    (size_t)kSmemBytes, st, tcodes, tpe, tcodes64, tpe64, a);
+  PartialArgs args = a;
+  args.cluster_merge = 0;
+  const int s = a.num_splits;
+  if (a.counters && s >= 2 && s <= kMaxClusterSplits) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        sms > 0) {
+      const long maxc = mla_max_clusters(dev, s);
+      if (maxc > 0 && (a.batch + maxc - 1) / maxc <= ((long)a.batch * s + sms - 1) / sms)
+        args.cluster_merge = 1;
+    } else {
+      (void)cudaGetLastError();
+    }
+  }
+  if (args.cluster_merge)
+    return launch_pdl_cluster(mla_tc_kernel, dim3(a.batch, s), dim3(kThreads),
+                              (size_t)kSmemBytes, s, st, tcodes, tpe, tcodes64, tpe64, args);
+  return launch_pdl(mla_tc_kernel, dim3(a.batch, s), dim3(kThreads), (size_t)kSmemBytes, st,
+                    tcodes, tpe, tcodes64, tpe64, args);
 }
 
 }  // namespace kvq

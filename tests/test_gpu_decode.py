@@ -330,6 +330,18 @@ def test_mla_fused(mla, s):
     assert not ws.counters.any()
 
 
+@pytest.mark.parametrize("s", [2, 3, 4, 8, 9])
+def test_mla_fused_equals_two_launches(mla, s):
+    """The fused MLA decode (2..8 splits: clusters merging through
+    distributed shared memory; 9: the last CTA's merge) gives the two-launch
+    result bit for bit, in fp32 and bf16, and leaves the counters at zero."""
+    for out in ("f32", "bf16"):
+        a, _ = mla.gpu_decode(s, out)
+        b, ws = fused(mla, s, out)
+        assert torch.equal(a, b), (s, out)
+        assert not ws.counters.any()
+
+
 def test_mla_paged_bf16_out():
     w = synth.mla_nvfp4(B=2, L=200)
     w.seq_lens = np.array([200, 129], np.int32)
