@@ -38,8 +38,13 @@
 // A 128-token tile fills the M = 128 rows of every S^T MMA (a 64-token tile
 // left half of them empty): 68 MMAs per 128 tokens instead of 104.  The
 // f16 tile is single buffered; rope tiles, S^T accumulators and P^T are
-// double buffered.  Every wait is bounded; a timeout sets an error bit and
-// the partials become NaN.
+// double buffered.  The softmax and decode loops start with a dry pass of
+// their code (nothing waited for, nothing handed over, the state unchanged)
+// while tile 0 is loaded: after an L2 flush their first real pass would
+// otherwise fetch the unrolled instructions from DRAM on the critical path.
+// With 2..8 splits the CTAs of a request form a cluster and merge their
+// partials through distributed shared memory.  Every wait is bounded; a
+// timeout sets an error bit and the partials become NaN.
 
 #include <atomic>
 
@@ -490,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // masked tokens of the O^T MMA).
     auto decode_block = [&](int x, int blk) {
       const uint32_t st = base + kOffRaw;
-      const int nvalid = min(kT, ntok - x * kT);
+      const int nvalid = x < 0 ? kT : min(kT, ntok - x * kT);
 #pragma unroll 1
       for (int u = dt; u < kT * 4; u += kDecoders) {
         const int p = u & 7, rest = u >> 3;
@@ -526,20 +531,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                  o[k][3]);
       }
       fence_proxy_async_shared();   // generic stores -> operands of the async MMAs
-      mbar_arrive(smem_u32(&sm.dec_blk[blk]));
+      if (x >= 0) mbar_arrive(smem_u32(&sm.dec_blk[blk]));
     };
 
     int issued = nt > 0 ? 1 : 0;
-    for (int x = 0; x < nt && !*abort_flag; ++x) {
-      wait_bar(smem_u32(&sm.raw_full), x & 1, abort_flag);
-      for (int blk = 0; blk < kBlocks && !*abort_flag; ++blk) {
+    // x = -1 is a dry pass: one block of whatever the raw buffer holds is
+    // decoded into the tile buffer (rewritten by tile 0 before any MMA reads
+    // it), with no wait and no arrival, so that the decode code is fetched
+    // while tile 0's codes are still on their way
+    for (int x = nt > 0 ? -1 : 0; x < nt && !*abort_flag; ++x) {
+      if (x >= 0) wait_bar(smem_u32(&sm.raw_full), x & 1, abort_flag);
+#pragma unroll 1
+      for (int blk = 0; blk < (x < 0 ? 1 : kBlocks) && !*abort_flag; ++blk) {
         // block blk of the tile buffer was last read by O^T x - 1 (and S^T
         // x - 1, which completed before it)
         if (x > 0) wait_bar(smem_u32(&sm.o_blk[blk]), (x - 1) & 1, abort_flag);
         decode_block(x, blk);
       }
       // the raw buffer is free once every decode thread is done with tile x
-      if (tma_thread && issued < nt) {
+      if (x >= 0 && tma_thread && issued < nt) {
         wait_bar(smem_u32(&sm.dec_blk[kBlocks - 1]), x & 1, abort_flag);
         if (!*abort_flag) issue_raw(issued++);
       }
@@ -560,20 +570,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int h = 0; h < kMlaHeads; ++h) m[h] = -INFINITY, l[h] = 0.f;
   if (warp < kSoftWarps) {
     // ============================================================ softmax
-    asm volatile("bar.sync 2, %0;" ::"n"(kDecoders + 32 * kSoftWarps) : "memory");
     float qf[kMlaHeads];
 #pragma unroll
-    for (int h = 0; h < kMlaHeads; ++h) qf[h] = sm.qfac[h];
+    for (int h = 0; h < kMlaHeads; ++h) qf[h] = 0.f;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
-    for (int t = 0; t < nt; ++t) {
-      wait_bar(smem_u32(&sm.s_done[t & 1]), (t >> 1) & 1, abort_flag);
+    // t = -1 is a dry pass of the loop's code while tile 0 is loaded and
+    // decoded (after the L2 flush its first run would fetch the unrolled
+    // instructions from DRAM when the first scores wait): every token is
+    // masked, so m and l do not move, and nothing is handed over.
+    for (int t = -1; t < nt; ++t) {
+      if (t == 0) {
+        asm volatile("bar.sync 2, %0;" ::"n"(kDecoders + 32 * kSoftWarps) : "memory");
+#pragma unroll
+        for (int h = 0; h < kMlaHeads; ++h) qf[h] = sm.qfac[h];
+      }
+      if (t >= 0) wait_bar(smem_u32(&sm.s_done[t & 1]), (t >> 1) & 1, abort_flag);
       tc_fence_after();
       uint32_t sl[16], sp[16];
       tmem_ld16(lane_addr + kColSLat + 16 * (t & 1), sl);
       tmem_ld16(lane_addr + kColSPe + 16 * (t & 1), sp);
       tmem_wait_ld();
       const int r = tid;   // token of the tile
-      const bool valid = r < ntok - t * kT && !*abort_flag;
+      const bool valid = t >= 0 && r < ntok - t * kT && !*abort_flag;
       float xs[kMlaHeads];
       bool need = false;
 #pragma unroll
@@ -585,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       need = __any_sync(0xffffffffu, need);
       if (lane == 0) sm.need[warp] = need;
       asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftWarps) : "memory");
-      const bool any_need = sm.need[0] | sm.need[1] | sm.need[2] | sm.need[3];
+      const bool any_need = t < 0 || (sm.need[0] | sm.need[1] | sm.need[2] | sm.need[3]);
       bool resc = false;
       float alpha[kMlaHeads];
       if (any_need) {
@@ -637,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_shared();
       tc_fence_before();
       asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftWarps) : "memory");   // all of P^T and O
-      if (tid == 0) mbar_arrive(smem_u32(&sm.p_ready[t & 1]));   // O^T MMAs t may go
+      if (tid == 0 && t >= 0) mbar_arrive(smem_u32(&sm.p_ready[t & 1]));   // O^T MMAs t may go
       if (*abort_flag) break;
     }
     // denominators over the tile's tokens; the reference max
