@@ -342,6 +342,22 @@ def test_mla_fused_equals_two_launches(mla, s):
         assert not ws.counters.any()
 
 
+def test_mla_fused_many_requests():
+    """38 requests x 4 splits: more four-CTA clusters than fit on a GB300 at
+    once (36), so the launcher keeps single CTAs and the last CTA's merge; the
+    result is still the two-launch one bit for bit, and matches the oracle."""
+    w = synth.mla_nvfp4(B=38, L=160)
+    w.seq_lens = (np.arange(38, dtype=np.int32) * 7) % 161
+    S = Setup(w)
+    a, _ = S.gpu_decode(4, "bf16")
+    b, ws = fused(S, 4, "bf16")
+    assert torch.equal(a, b)
+    assert not ws.counters.any()
+    ref, _ = S.oracle_decode()
+    out, _ = fused(S, 4)
+    assert_f32_close(out.cpu().numpy(), ref, "mla 38 requests fused")
+
+
 def test_mla_paged_bf16_out():
     w = synth.mla_nvfp4(B=2, L=200)
     w.seq_lens = np.array([200, 129], np.int32)
