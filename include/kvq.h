@@ -23,7 +23,8 @@
  * Conventions (all calls):
  *  - Every device buffer (cache, queries, outputs, workspace) is allocated
  *    and owned by the caller.  The library allocates no memory and keeps no
- *    per-call state; calls are re-entrant.
+ *    per-call state; calls are re-entrant.  (It caches, per device, values
+ *    that do not change: the number of MLA CTA clusters that fit at once.)
  *  - Pointers marked (device) must be device (or managed) memory of the
  *    current CUDA device; pointers marked (host) are read on the host.  The
  *    per-step inputs read with plain loads -- q, k_new, v_new, kpe_new --

@@ -334,10 +334,11 @@ def test_mla_fused(mla, s):
 def test_mla_fused_equals_two_launches(mla, s):
     """The fused MLA decode (2..8 splits: clusters merging through
     distributed shared memory; 9: the last CTA's merge) gives the two-launch
-    result bit for bit, in fp32 and bf16, and leaves the counters at zero."""
-    for out in ("f32", "bf16"):
-        a, _ = mla.gpu_decode(s, out)
-        b, ws = fused(mla, s, out)
+    result bit for bit, in fp32, bf16 and E4M3, and leaves the counters at
+    zero."""
+    for out, scale in (("f32", 1.0), ("bf16", 1.0), ("e4m3", 0.01)):
+        a, _ = mla.gpu_decode(s, out, scale)
+        b, ws = fused(mla, s, out, scale)
         assert torch.equal(a, b), (s, out)
         assert not ws.counters.any()
 
