@@ -496,39 +496,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto decode_block = [&](int x, int blk) {
       const uint32_t st = base + kOffRaw;
       const int nvalid = x < 0 ? kT : min(kT, ntok - x * kT);
-#pragma unroll 1
-      for (int u = dt; u < kT * 4; u += kDecoders) {
+      // this thread's units u = dt + k kDecoders (up to kUnits): every load
+      // first, then the conversions and stores, so the loads overlap
+      constexpr int kUnits = (kT * 4 + kDecoders - 1) / kDecoders;
+      uint4 v[kUnits];
+      uint32_t sc[kUnits];
+#pragma unroll
+      for (int k = 0; k < kUnits; ++k) {
+        const int u = dt + k * kDecoders;
         const int p = u & 7, rest = u >> 3;
-        const int rg = rest >> 2, db = 2 * blk + ((rest >> 1) & 1), half = rest & 1;
-        const int r = rg * 8 + p;
+        const int db = 2 * blk + ((rest >> 1) & 1), half = rest & 1;
+        const int r = (rest >> 2) * 8 + p;
+        v[k] = make_uint4(0u, 0u, 0u, 0u);
+        sc[k] = 0u;
+        if (u < kT * 4 && r < nvalid) {
+          v[k] = lds128(st + (db >> 2) * kHalfBytes + r * 128 +
+                        (((((db & 3) * 2 + half) ^ r) & 7) << 4));
+          sc[k] = lds16(st + kRawCodes + r * (kMlaLat / 16) + db * 4 + half * 2);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kUnits; ++k) {
+        const int u = dt + k * kDecoders;
+        if (u >= kT * 4) break;
+        const int p = u & 7, rest = u >> 3;
+        const int db = 2 * blk + ((rest >> 1) & 1), half = rest & 1;
+        const int r = (rest >> 2) * 8 + p;
+        // rows past the chunk: zero codes and scales decode to zeros
+        const uint32_t s2 = e4m3x2_to_f16x2(sc[k]);
+        const uint32_t s_lo = __byte_perm(s2, 0, 0x1010), s_hi = __byte_perm(s2, 0, 0x3232);
+        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
         uint32_t o[4][4];
-        if (r < nvalid) {
-          const uint4 v = lds128(st + (db >> 2) * kHalfBytes + r * 128 +
-                                 (((((db & 3) * 2 + half) ^ r) & 7) << 4));
-          const uint32_t sc = lds16(st + kRawCodes + r * (kMlaLat / 16) + db * 4 + half * 2);
-          const uint32_t s2 = e4m3x2_to_f16x2(sc);
-          const uint32_t s_lo = __byte_perm(s2, 0, 0x1010), s_hi = __byte_perm(s2, 0, 0x3232);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint32_t e0, e1, e2, e3;
-            e2m1x8_to_f16x2x4(w[k], e0, e1, e2, e3);
-            const uint32_t s = k < 2 ? s_lo : s_hi;
-            o[k][0] = hmul2(e0, s);
-            o[k][1] = hmul2(e1, s);
-            o[k][2] = hmul2(e2, s);
-            o[k][3] = hmul2(e3, s);
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0u;
+        for (int j = 0; j < 4; ++j) {
+          uint32_t e0, e1, e2, e3;
+          e2m1x8_to_f16x2x4(w[j], e0, e1, e2, e3);
+          const uint32_t sj = j < 2 ? s_lo : s_hi;
+          o[j][0] = hmul2(e0, sj);
+          o[j][1] = hmul2(e1, sj);
+          o[j][2] = hmul2(e2, sj);
+          o[j][3] = hmul2(e3, sj);
         }
         const uint32_t row_base =
             base + kOffTile + db * kColBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          sts128(row_base + ((((half * 4 + k) ^ r) & 7) << 4), o[k][0], o[k][1], o[k][2],
-                 o[k][3]);
+        for (int j = 0; j < 4; ++j)
+          sts128(row_base + ((((half * 4 + j) ^ r) & 7) << 4), o[j][0], o[j][1], o[j][2],
+                 o[j][3]);
       }
       fence_proxy_async_shared();   // generic stores -> operands of the async MMAs
       if (x >= 0) mbar_arrive(smem_u32(&sm.dec_blk[blk]));
