@@ -528,7 +528,7 @@ __device__ __forceinline__ void fused_combine_staged(const PartialArgs& a, int b
 // Merge through distributed shared memory, for a launch in clusters of the
 // s <= 8 splits of a request (cluster rank = split): every CTA holds its
 // normalized partial [rows][Dv] fp32 at shared address `own` and its lse
-// [rows] at `own_lse`.  After a cluster barrier one thread per row forms the
+// [rows] at `own_lse`.  After a cluster barrier eight lanes per row form the
 // row's weights from the peers' lse, and CTA rank r computes items
 // [r n / s, (r + 1) n / s) of the n = rows Dv / 4 (row, 4 value dims) items,
 // loading each item's s partials from the peers' shared memory in one round;
@@ -583,21 +583,23 @@ __device__ __forceinline__ void fused_combine_cluster(const PartialArgs& a, size
   cluster_sync_all();   // every split's partial and lse are written
   const int s = a.num_splits;
   float* winv = wbuf + kMaxGroup * kMaxFusedSplits;
-  if ((int)threadIdx.x < rows) {
-    const int r = threadIdx.x;
-    float lv[kMaxClusterSplits];
-    float M = -INFINITY;
+  // weights: eight lanes per row, lane j for split j (lse -inf for j >= s);
+  // the xor-4/2/1 butterfly of (own + other) leaves lane 0 of the group with
+  // ((e0 + e4) + (e2 + e6)) + ((e1 + e5) + (e3 + e7))
+  if ((int)threadIdx.x < ((rows * kMaxClusterSplits + 31) & ~31)) {
+    const int r = (int)threadIdx.x / kMaxClusterSplits, j = (int)threadIdx.x % kMaxClusterSplits;
+    const bool in = r < rows && j < s;
+    const float lv = in ? ld_cluster_f32(cluster_map(own_lse + 4u * r, j)) : -INFINITY;
+    float M = lv;
 #pragma unroll
-    for (int j = 0; j < kMaxClusterSplits; ++j) {
-      lv[j] = j < s ? ld_cluster_f32(cluster_map(own_lse + 4u * r, j)) : -INFINITY;
-      M = fmaxf(M, lv[j]);
-    }
-    float* wr = wbuf + r * kMaxFusedSplits;
-#pragma unroll 1
-    for (int j = 0; j < kMaxClusterSplits; ++j)
-      wr[j] = (j >= s || M == -INFINITY || lv[j] == -INFINITY) ? 0.f : expf(lv[j] - M);
-    const float sum = ((wr[0] + wr[4]) + (wr[2] + wr[6])) + ((wr[1] + wr[5]) + (wr[3] + wr[7]));
-    winv[r] = sum > 0.f ? 1.f / sum : (sum == 0.f ? 0.f : NAN);
+    for (int o = kMaxClusterSplits / 2; o > 0; o >>= 1)
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float e = (M == -INFINITY || lv == -INFINITY) ? 0.f : expf(lv - M);
+    if (in) wbuf[r * kMaxFusedSplits + j] = e;
+    float sum = e;
+#pragma unroll
+    for (int o = kMaxClusterSplits / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (r < rows && j == 0) winv[r] = sum > 0.f ? 1.f / sum : (sum == 0.f ? 0.f : NAN);
   }
   __syncthreads();
   if (a.out_dtype == 0)
