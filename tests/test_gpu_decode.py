@@ -330,10 +330,11 @@ def test_mla_fused(mla, s):
     assert not ws.counters.any()
 
 
-@pytest.mark.parametrize("s", [2, 3, 4, 8, 9])
+@pytest.mark.parametrize("s", [2, 3, 4, 5, 6, 7, 8, 9])
 def test_mla_fused_equals_two_launches(mla, s):
     """The fused MLA decode (2..8 splits: clusters merging through
-    distributed shared memory; 9: the last CTA's merge) gives the two-launch
+    distributed shared memory, whose item ranges split rows for 3, 5, 6
+    and 7; 9: the last CTA's merge) gives the two-launch
     result bit for bit, in fp32, bf16 and E4M3, and leaves the counters at
     zero."""
     for out, scale in (("f32", 1.0), ("bf16", 1.0), ("e4m3", 0.01)):
